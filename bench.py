@@ -1,0 +1,438 @@
+"""Benchmark: MoE expert-parallel dispatch + combine on B300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload capacity] [--payload int8|bf16]
+    python bench.py --impl reference ...      # the CPU oracle on a bounded sample
+
+A step is one pass of the whole path over one batch: ep_route -> ep_dispatch
+-> ep_combine on one stream, inputs resident in HBM. The headline workload is
+T=16384 tokens, H=4096, E=128 experts, top-8, R=8 virtual ranks, capacity
+factor 1.25, int8 payload. The metric is tokens/s; achieved HBM GB/s on the
+algorithmic bytes (logits + x + payload + scales + expert outputs + y) is
+reported beside it as a fraction of both the nominal 8 TB/s and the measured
+copy bandwidth.
+
+Under torchrun (N>1) every rank runs an independent replica of the workload
+on its own GPU (the path has no exchange step on one node: its R ranks are
+virtual), timing takes the max over ranks, and `value` counts all ranks'
+tokens. Rank 0 prints one JSON line.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+from pathlib import Path
+
+ROOT = Path(__file__).resolve().parent
+if str(ROOT) not in sys.path:
+    sys.path.insert(0, str(ROOT))
+
+NOMINAL_HBM_GBS = 8000.0
+FALLBACK_HBM_GBS = 6400.0
+L2_BYTES = 126 * 1024 * 1024
+METRIC = "dispatch+combine tokens/s and HBM GB/s as % of B300 peak (T=16384,H=4096)"
+TRAFFIC_FILE = ROOT / "profiles" / "roofline_traffic.json"
+
+
+# ----------------------------------------------------------------------------
+# algorithmic bytes (per step, per kernel)
+# ----------------------------------------------------------------------------
+def algorithmic_bytes(T, H, E, k, N, payload_int8, out_int8=False):
+    """Bytes each stage must move at least once, with N dispatched rows.
+
+    route:    logits T*E*4 read
+    dispatch: x T*H*2 read; payload N*H*b written (+ scales N*4 in int8)
+    combine:  expert outputs N*H*b_out read (+ N*4 scales if int8); y T*H*2 written
+    Routing metadata (indices, weights, slot maps: ~16*T*k bytes) is kept apart.
+    """
+    b = 1 if payload_int8 else 2
+    b_out = 1 if out_int8 else 2
+    route = T * E * 4
+    dispatch = T * H * 2 + N * H * b + (N * 4 if payload_int8 else 0)
+    combine = N * H * b_out + (N * 4 if out_int8 else 0) + T * H * 2
+    meta = T * k * 4 * 4
+    return dict(route=route, dispatch=dispatch, combine=combine, total=route + dispatch + combine, metadata=meta)
+
+
+def measured_peak_gbs():
+    p = ROOT / "MEASURED_PEAKS.json"
+    try:
+        d = json.loads(p.read_text())
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def source_digest(paths):
+    h = hashlib.sha256()
+    for p in paths:
+        h.update(Path(p).read_bytes())
+    return h.hexdigest()[:16]
+
+
+KERNEL_SOURCES = {
+    "combine": ["combine_warp_top_fp32_b300/csrc/combine.cu", "combine_warp_top_fp32_b300/csrc/ep_device.cuh"],
+    "dispatch": ["combine_warp_top_fp32_b300/csrc/dispatch.cu", "combine_warp_top_fp32_b300/csrc/ep_device.cuh"],
+    "route": ["combine_warp_top_fp32_b300/csrc/route.cu"],
+}
+
+
+def recorded_traffic(kernel, workload, payload):
+    """DRAM bytes per launch from an ncu capture, only if the kernel's sources
+    are unchanged since that capture (else None)."""
+    try:
+        d = json.loads(TRAFFIC_FILE.read_text())
+        rec = d[f"{kernel}/{workload}/{payload}"]
+        if rec["source_digest"] != source_digest(ROOT / p for p in KERNEL_SOURCES[kernel]):
+            return None
+        return int(rec["dram_bytes_per_launch"])
+    except Exception:
+        return None
+
+
+# ----------------------------------------------------------------------------
+# clocks during the timed region
+# ----------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.dev = device_index
+        self.proc = None
+        self.lines = []
+        self.error = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.dev), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+            time.sleep(0.3)
+        except Exception as e:  # no nvidia-smi: report why
+            self.error = f"nvidia-smi unavailable: {e}"
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"error": self.error}
+        time.sleep(0.2)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx = float(parts[1])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[3:7]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"error": "no clock samples"}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "samples": len(sm), "reasons": sorted(reasons)}
+
+
+# ----------------------------------------------------------------------------
+# distributed plumbing (replicas only)
+# ----------------------------------------------------------------------------
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def max_over_ranks(value: float, group=None) -> float:
+    """The slowest rank's time (a no-op without an initialised process group)."""
+    import torch
+    import torch.distributed as dist
+
+    if not (dist.is_available() and dist.is_initialized()):
+        return value
+    backend = dist.get_backend(group)
+    dev = torch.device("cuda", torch.cuda.current_device()) if backend == "nccl" else torch.device("cpu")
+    t = torch.tensor([value], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX, group=group)
+    return float(t.item())
+
+
+def barrier():
+    import torch.distributed as dist
+
+    if dist.is_available() and dist.is_initialized():
+        dist.barrier()
+
+
+# ----------------------------------------------------------------------------
+# CPU oracle timing (reference arm and the cpu_baseline leg)
+# ----------------------------------------------------------------------------
+def oracle_sample_tokens(w, target_s=2.0, probe_tokens=256):
+    """Tokens per oracle step so that one step takes about target_s seconds."""
+    t = oracle_pass_seconds(w, min(probe_tokens, w.T))
+    per_token = t / min(probe_tokens, w.T)
+    return max(1, min(w.T, int(target_s / max(per_token, 1e-9))))
+
+
+_oracle_cache = {}
+
+
+def _oracle_inputs(w, n_tokens):
+    import torch
+
+    from combine_warp_top_fp32_b300 import workloads
+
+    key = (w.name, n_tokens)
+    if key not in _oracle_cache:
+        ws = w.replace(T=n_tokens)
+        d = workloads.generate(ws, device="cpu")
+        _oracle_cache.clear()
+        _oracle_cache[key] = (ws, d["logits"].numpy(), workloads.bf16_bits(d["x"]), workloads.bf16_bits(d["expert_out"]))
+    return _oracle_cache[key]
+
+
+def oracle_pass_seconds(w, n_tokens, payload_int8=None):
+    import oracle
+
+    ws, logits, x_bits, eo_bits = _oracle_inputs(w, n_tokens)
+    orc = oracle.Oracle()
+    p8 = (w.payloads[0] == 1) if payload_int8 is None else payload_int8
+    t0 = time.perf_counter()
+    orc.forward(logits, x_bits, eo_bits, ws.k, ws.R, ws.capacity_factor, ws.renormalize, p8)
+    return time.perf_counter() - t0
+
+
+def run_reference(args):
+    ws_, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    from combine_warp_top_fp32_b300 import workloads
+
+    w = workloads.WORKLOADS[args.workload]
+    p8 = args.payload == "int8"
+    n = oracle_sample_tokens(w, target_s=args.reference_step_s)
+    for _ in range(args.warmup):
+        oracle_pass_seconds(w, n, p8)
+    times = [oracle_pass_seconds(w, n, p8) for _ in range(args.steps)]
+    total = sum(times)
+    value = n * args.steps / total
+    cores = 1
+    sample = f"first {n} of {w.T} tokens of the '{w.name}' workload per step (an instance of the same shape with T={n})"
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "fp32",
+        "data": "synthetic", "config": workload_config(w, args.payload, None),
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle", "sample": sample,
+                         "cpu": cpu_model()},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+    return 0
+
+
+def cpu_model():
+    try:
+        for ln in Path("/proc/cpuinfo").read_text().splitlines():
+            if ln.startswith("model name"):
+                return ln.split(":", 1)[1].strip() + f" (nproc={os.cpu_count()})"
+    except Exception:
+        pass
+    return f"unknown (nproc={os.cpu_count()})"
+
+
+def workload_config(w, payload, n_rows):
+    return {"workload": w.name, "T": w.T, "H": w.H, "E": w.E, "k": w.k, "R": w.R,
+            "capacity_factor": w.capacity_factor, "cap": w.capacity() if w.capacity_factor > 0 else None,
+            "payload": payload, "expert_out": "bf16", "rows_dispatched": n_rows,
+            "l2": "no flush: each step moves > 1 GB, far beyond the 126 MB L2",
+            "parallelism": "replicas (R virtual ranks per GPU)"}
+
+
+# ----------------------------------------------------------------------------
+# the GPU arm
+# ----------------------------------------------------------------------------
+def run_gpu(args):
+    import torch
+    import torch.distributed as dist
+
+    world, rank, local = dist_env()
+    if world > 1:
+        dist.init_process_group("nccl", init_method="env://")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+
+    from combine_warp_top_fp32_b300 import binding as ep
+    from combine_warp_top_fp32_b300 import workloads
+
+    w = workloads.WORKLOADS[args.workload]
+    p8 = args.payload == "int8"
+    cfg = ep.config_from_workload(w, payload=ep.EP_PAYLOAD_INT8 if p8 else ep.EP_PAYLOAD_BF16)
+    d = workloads.generate(w, device=dev)
+    logits, x, eo = d["logits"], d["x"], d["expert_out"]
+    buf = ep.EpBuffers.allocate(cfg)
+    stream = torch.cuda.current_stream()
+
+    for _ in range(args.warmup):
+        buf.step(logits, x, eo)
+    torch.cuda.synchronize()
+    assert ep.ep_get_error(buf.ws) == ep.EP_OK
+    N = int(buf.rank_off[-1].item())
+    launches_per_step = 5 if w.T > 0 else 1
+
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    sampler = ClockSampler(local)
+    sampler.start()
+    barrier()
+    torch.cuda.synchronize()
+    for i in range(args.steps):
+        e = ev[i]
+        e[0].record(stream)
+        buf.route(logits)
+        e[1].record(stream)
+        buf.dispatch(x)
+        e[2].record(stream)
+        buf.combine(eo)
+        e[3].record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    clocks = sampler.stop()
+    total_ms = ev[0][0].elapsed_time(ev[-1][3])
+    stage_ms = {
+        "route": sum(e[0].elapsed_time(e[1]) for e in ev) / args.steps,
+        "dispatch": sum(e[1].elapsed_time(e[2]) for e in ev) / args.steps,
+        "combine": sum(e[2].elapsed_time(e[3]) for e in ev) / args.steps,
+    }
+    total_s = max_over_ranks(total_ms / 1e3)
+    ms_per_step = 1e3 * total_s / args.steps
+    tokens = w.T * args.steps * world
+    value = tokens / total_s
+
+    nb = algorithmic_bytes(w.T, w.H, w.E, w.k, N, p8)
+    peak, peak_src = measured_peak_gbs()
+    step_gbs = nb["total"] / (ms_per_step / 1e3) / 1e9
+    stage_gbs = {s: nb[s] / (stage_ms[s] / 1e3) / 1e9 for s in stage_ms}
+    dominant = max(stage_ms, key=stage_ms.get)
+    kernel_names = {"route": "route_topk_kernel", "dispatch": "count+scan+scatter_kernel",
+                    "combine": "combine_kernel<bf16>"}
+    traffic = recorded_traffic(dominant, w.name, args.payload)
+
+    # end to end through the public API with host buffers: pinned H2D of the
+    # step's inputs, the three calls, D2H of the result, every step
+    e2e = None
+    if not args.no_e2e:
+        h_logits = logits.cpu().pin_memory()
+        h_x = x.cpu().pin_memory()
+        h_eo = eo.cpu().pin_memory()
+        h_y = torch.empty(buf.y.shape, dtype=buf.y.dtype).pin_memory()
+        d_logits, d_x, d_eo = torch.empty_like(logits), torch.empty_like(x), torch.empty_like(eo)
+
+        def e2e_step():
+            d_logits.copy_(h_logits, non_blocking=True)
+            d_x.copy_(h_x, non_blocking=True)
+            d_eo.copy_(h_eo, non_blocking=True)
+            buf.step(d_logits, d_x, d_eo)
+            h_y.copy_(buf.y, non_blocking=True)
+
+        for _ in range(max(1, min(args.warmup, 3))):
+            e2e_step()
+        torch.cuda.synchronize()
+        k2 = max(1, min(args.steps, args.e2e_steps))
+        barrier()
+        s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s0.record(stream)
+        for _ in range(k2):
+            e2e_step()
+        s1.record(stream)
+        torch.cuda.synchronize()
+        barrier()
+        e2e_s = max_over_ranks(s0.elapsed_time(s1) / 1e3)
+        h2d = logits.numel() * 4 + x.numel() * 2 + eo.numel() * 2
+        e2e = {"value": w.T * k2 * world / e2e_s, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": buf.y.numel() * 2, "steps": k2,
+               "note": "inputs = logits + x + synthetic expert outputs (all max_rows rows)"}
+
+    cpu_baseline = None
+    if rank == 0 and not args.no_cpu_baseline:
+        n = oracle_sample_tokens(w, target_s=args.cpu_baseline_s / 3)
+        reps = 3
+        secs = sum(oracle_pass_seconds(w, n, p8) for _ in range(reps))
+        cpu_baseline = {"value": n * reps / secs, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+                        "sample": f"{reps} passes over the first {n} of {w.T} tokens (same shape, T={n})",
+                        "cpu": cpu_model()}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "fp32", "data": "synthetic", "config": workload_config(w, args.payload, N),
+            "hbm": {"bytes_per_step": nb["total"], "gbs": step_gbs, "frac_of_8000": step_gbs / NOMINAL_HBM_GBS,
+                    f"frac_of_{peak_src}": step_gbs / peak, "metadata_bytes_per_step": nb["metadata"]},
+            "stages": {s: {"ms": stage_ms[s], "bytes": nb[s], "gbs": stage_gbs[s]} for s in stage_ms},
+            "roofline": {"bound": "hbm", "kernel": kernel_names[dominant], "achieved": stage_gbs[dominant],
+                         "peak": peak, "unit": "GB/s", "frac": stage_gbs[dominant] / peak, "traffic": traffic,
+                         "algorithmic_bytes_per_launch": nb[dominant], "peak_source": peak_src},
+            "clocks": clocks,
+            "gpu_launches": launches_per_step * args.steps,
+            "e2e": e2e,
+            "cpu_baseline": cpu_baseline,
+        }
+        print(json.dumps(line))
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+def parse_args(argv=None):
+    ap = argparse.ArgumentParser(description="MoE dispatch+combine benchmark")
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="capacity")
+    ap.add_argument("--payload", choices=["int8", "bf16"], default=None)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--e2e-steps", type=int, default=10)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-baseline-s", type=float, default=15.0)
+    ap.add_argument("--reference-step-s", type=float, default=2.0)
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    from combine_warp_top_fp32_b300 import workloads
+
+    w = workloads.WORKLOADS[args.workload]
+    if args.payload is None:
+        args.payload = "int8" if w.payloads[0] == 1 else "bf16"
+    return args
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_gpu(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

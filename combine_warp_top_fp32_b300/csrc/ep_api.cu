@@ -1,0 +1,238 @@
+// ep_api.cu — the extern "C" entry points of libep_b300 (declared in ep.h):
+// host-side argument checks, workspace carving and kernel launches.
+//
+// Every check runs before the first launch, so a call that returns
+// EP_ERR_INVALID_ARG or EP_ERR_WORKSPACE has enqueued nothing. The library
+// never synchronises a stream except in ep_get_error().
+#include <math.h>
+#include <string.h>
+
+#include "ep.h"
+#include "ep_internal.h"
+
+namespace {
+
+constexpr int kMaxH = 16384;
+constexpr int kMaxE = 1024;
+constexpr int kMaxK = 32;
+constexpr int kMaxDevices = 64;
+
+int g_sm_count[kMaxDevices];  // per-device SM count, filled on first use
+
+// SM count of the current device (cached); 0 on failure.
+int current_sm_count() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return 0;
+  if (dev < kMaxDevices && g_sm_count[dev] > 0) return g_sm_count[dev];
+  int sms = 0;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+  if (dev < kMaxDevices) g_sm_count[dev] = sms;
+  return sms;
+}
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+bool config_ok(const ep_config_t* c) {
+  if (c == nullptr) return false;
+  if (c->T < 0) return false;
+  if (c->H < 16 || c->H > kMaxH || c->H % 16 != 0) return false;
+  if (c->E < 1 || c->E > kMaxE) return false;
+  if (c->k < 1 || c->k > c->E || c->k > kMaxK) return false;
+  if (c->R < 1 || c->E % c->R != 0) return false;
+  if (isnan(c->capacity_factor) || isinf(c->capacity_factor)) return false;
+  if (c->renormalize != 0 && c->renormalize != 1) return false;
+  if (c->payload != EP_PAYLOAD_BF16 && c->payload != EP_PAYLOAD_INT8) return false;
+  if (static_cast<int64_t>(c->T) * c->k > INT32_MAX) return false;
+  return true;
+}
+
+// ceil(cf * T * k / E) in double, in that order, clipped to T (an expert can
+// receive at most one copy per token); T when dropless.
+int32_t capacity_of(const ep_config_t* c) {
+  if (!(c->capacity_factor > 0.0f)) return c->T;
+  const double v = ceil(static_cast<double>(c->capacity_factor) * c->T * c->k / c->E);
+  return v >= static_cast<double>(c->T) ? c->T : static_cast<int32_t>(v);
+}
+
+int64_t max_rows_of(const ep_config_t* c) {
+  const int64_t tk = static_cast<int64_t>(c->T) * c->k;
+  if (!(c->capacity_factor > 0.0f)) return tk;
+  const int64_t ecap = static_cast<int64_t>(c->E) * capacity_of(c);
+  return tk < ecap ? tk : ecap;
+}
+
+ep_status_t from_cuda(cudaError_t e) { return e == cudaSuccess ? EP_OK : EP_ERR_CUDA; }
+
+}  // namespace
+
+extern "C" {
+
+const char* ep_status_string(ep_status_t s) {
+  switch (s) {
+    case EP_OK: return "ok";
+    case EP_ERR_INVALID_ARG: return "invalid argument";
+    case EP_ERR_WORKSPACE: return "workspace missing or too small";
+    case EP_ERR_CUDA: return "CUDA runtime error";
+    case EP_ERR_TIMEOUT: return "bounded device wait timed out";
+    case EP_ERR_DEVICE_INDEX: return "index input out of range or repeated";
+  }
+  return "unknown status";
+}
+
+ep_status_t ep_config_check(const ep_config_t* cfg) { return config_ok(cfg) ? EP_OK : EP_ERR_INVALID_ARG; }
+
+ep_status_t ep_capacity(const ep_config_t* cfg, int32_t* cap) {
+  if (!config_ok(cfg) || cap == nullptr) return EP_ERR_INVALID_ARG;
+  *cap = capacity_of(cfg);
+  return EP_OK;
+}
+
+int64_t ep_max_rows(const ep_config_t* cfg) { return config_ok(cfg) ? max_rows_of(cfg) : 0; }
+
+ep_status_t ep_workspace_size(const ep_config_t* cfg, size_t* bytes) {
+  if (!config_ok(cfg) || bytes == nullptr) return EP_ERR_INVALID_ARG;
+  *bytes = ep::ws_layout(cfg->T, cfg->E, cfg->k).total;
+  return EP_OK;
+}
+
+ep_status_t ep_workspace_init(void* ws, size_t ws_bytes, cudaStream_t stream) {
+  if (ws == nullptr || ws_bytes < 256 || !aligned(ws, 256)) return EP_ERR_WORKSPACE;
+  return from_cuda(cudaMemsetAsync(ws, 0, ws_bytes, stream));
+}
+
+ep_status_t ep_route(const ep_config_t* cfg, const float* logits, int32_t* topk_idx, float* topk_w,
+                     cudaStream_t stream) {
+  if (!config_ok(cfg)) return EP_ERR_INVALID_ARG;
+  if (cfg->T == 0) return EP_OK;
+  if (!logits || !topk_idx || !topk_w) return EP_ERR_INVALID_ARG;
+  if (!aligned(logits, 16) || !aligned(topk_idx, 4) || !aligned(topk_w, 4)) return EP_ERR_INVALID_ARG;
+  const int sms = current_sm_count();
+  if (sms <= 0) return EP_ERR_CUDA;
+  return from_cuda(ep::launch_route(logits, cfg->T, cfg->E, cfg->k, cfg->renormalize, topk_idx, topk_w, sms, stream));
+}
+
+ep_status_t ep_dispatch(const ep_config_t* cfg, const void* x, const int32_t* topk_idx, void* payload,
+                        float* scales, int32_t* row_slot, int32_t* slot_row, int32_t* expert_counts,
+                        int32_t* expert_raw, int32_t* expert_off, int32_t* rank_off, int32_t* n_dropped,
+                        void* ws, size_t ws_bytes, cudaStream_t stream) {
+  if (!config_ok(cfg)) return EP_ERR_INVALID_ARG;
+  const bool int8 = cfg->payload == EP_PAYLOAD_INT8;
+  if (!expert_counts || !expert_off || !rank_off || !n_dropped) return EP_ERR_INVALID_ARG;
+  if (cfg->T > 0) {
+    if (!x || !topk_idx || !payload || !row_slot || !slot_row) return EP_ERR_INVALID_ARG;
+    if (int8 && !scales) return EP_ERR_INVALID_ARG;
+    if (!aligned(x, 16) || !aligned(payload, 16)) return EP_ERR_INVALID_ARG;
+  }
+  if (!aligned(topk_idx, 4) || !aligned(row_slot, 4) || !aligned(slot_row, 4) || !aligned(expert_counts, 4) ||
+      !aligned(expert_raw, 4) || !aligned(expert_off, 4) || !aligned(rank_off, 4) || !aligned(n_dropped, 4) ||
+      !aligned(scales, 4))
+    return EP_ERR_INVALID_ARG;
+  const ep::WsLayout L = ep::ws_layout(cfg->T, cfg->E, cfg->k);
+  if (ws == nullptr || ws_bytes < L.total || !aligned(ws, 256)) return EP_ERR_WORKSPACE;
+  const int sms = current_sm_count();
+  if (sms <= 0) return EP_ERR_CUDA;
+
+  char* w = static_cast<char*>(ws);
+  ep::DispatchArgs a;
+  a.T = cfg->T;
+  a.H = cfg->H;
+  a.E = cfg->E;
+  a.k = cfg->k;
+  a.R = cfg->R;
+  a.cap = capacity_of(cfg);
+  a.int8 = int8 ? 1 : 0;
+  a.x = x;
+  a.topk_idx = topk_idx;
+  a.payload = payload;
+  a.scales = scales;
+  a.row_slot = row_slot;
+  a.slot_row = slot_row;
+  a.expert_counts = expert_counts;
+  a.expert_raw = expert_raw;
+  a.expert_off = expert_off;
+  a.rank_off = rank_off;
+  a.n_dropped = n_dropped;
+  a.status = reinterpret_cast<uint32_t*>(w + L.status_off);
+  a.tile_counts = reinterpret_cast<int32_t*>(w + L.tile_counts_off);
+  a.tile_base = reinterpret_cast<int32_t*>(w + L.tile_base_off);
+  a.lrank = reinterpret_cast<int32_t*>(w + L.lrank_off);
+  a.tile = L.tile;
+  a.ntiles = L.ntiles;
+  return from_cuda(ep::launch_dispatch(a, sms, stream));
+}
+
+ep_status_t ep_combine(const ep_config_t* cfg, const void* expert_out, const float* out_scales,
+                       int32_t out_payload, const int32_t* slot_row, const float* topk_w, void* y, void* ws,
+                       size_t ws_bytes, cudaStream_t stream) {
+  if (!config_ok(cfg)) return EP_ERR_INVALID_ARG;
+  if (out_payload != EP_PAYLOAD_BF16 && out_payload != EP_PAYLOAD_INT8) return EP_ERR_INVALID_ARG;
+  if (ws == nullptr || ws_bytes < 256 || !aligned(ws, 256)) return EP_ERR_WORKSPACE;
+  if (cfg->T == 0) return EP_OK;
+  const bool int8 = out_payload == EP_PAYLOAD_INT8;
+  if (!expert_out || !slot_row || !topk_w || !y || (int8 && !out_scales)) return EP_ERR_INVALID_ARG;
+  if (!aligned(expert_out, 16) || !aligned(y, 16) || !aligned(slot_row, 4) || !aligned(topk_w, 4) ||
+      !aligned(out_scales, 4))
+    return EP_ERR_INVALID_ARG;
+  const int sms = current_sm_count();
+  if (sms <= 0) return EP_ERR_CUDA;
+  ep::CombineArgs a;
+  a.T = cfg->T;
+  a.H = cfg->H;
+  a.k = cfg->k;
+  a.int8_out = int8 ? 1 : 0;
+  a.max_rows = max_rows_of(cfg);
+  a.expert_out = expert_out;
+  a.out_scales = out_scales;
+  a.slot_row = slot_row;
+  a.topk_w = topk_w;
+  a.y = y;
+  a.status = static_cast<uint32_t*>(ws);
+  return from_cuda(ep::launch_combine(a, sms, stream));
+}
+
+ep_status_t ep_quantize_rows(const void* in, int64_t n, int32_t H, int8_t* q, float* scales, cudaStream_t stream) {
+  if (n < 0 || H < 16 || H > kMaxH || H % 16 != 0) return EP_ERR_INVALID_ARG;
+  if (n == 0) return EP_OK;
+  if (!in || !q || !scales || !aligned(in, 16) || !aligned(q, 16) || !aligned(scales, 4)) return EP_ERR_INVALID_ARG;
+  const int sms = current_sm_count();
+  if (sms <= 0) return EP_ERR_CUDA;
+  return from_cuda(ep::launch_quantize_rows(in, n, H, q, scales, sms, stream));
+}
+
+ep_status_t ep_get_error(void* ws, size_t ws_bytes, cudaStream_t stream) {
+  if (ws == nullptr || ws_bytes < 256 || !aligned(ws, 256)) return EP_ERR_WORKSPACE;
+  uint32_t flags = 0;
+  if (cudaMemcpyAsync(&flags, ws, sizeof flags, cudaMemcpyDeviceToHost, stream) != cudaSuccess) return EP_ERR_CUDA;
+  if (cudaStreamSynchronize(stream) != cudaSuccess) return EP_ERR_CUDA;
+  if (flags == 0) return EP_OK;
+  if (cudaMemsetAsync(ws, 0, sizeof flags, stream) != cudaSuccess) return EP_ERR_CUDA;
+  if (flags & ep::kStatusTimeout) return EP_ERR_TIMEOUT;
+  return EP_ERR_DEVICE_INDEX;
+}
+
+ep_status_t ep_load_stats(const int32_t* host_counts, int32_t E, ep_load_stats_t* out) {
+  if (host_counts == nullptr || out == nullptr || E < 1) return EP_ERR_INVALID_ARG;
+  int64_t total = 0;
+  int32_t mn = host_counts[0], mx = host_counts[0];
+  for (int32_t e = 0; e < E; ++e) {
+    total += host_counts[e];
+    if (host_counts[e] < mn) mn = host_counts[e];
+    if (host_counts[e] > mx) mx = host_counts[e];
+  }
+  const double mean = static_cast<double>(total) / E;
+  double var = 0.0;
+  for (int32_t e = 0; e < E; ++e) {
+    const double d = host_counts[e] - mean;
+    var += d * d;
+  }
+  var /= E;
+  out->mean = mean;
+  out->stddev = sqrt(var);
+  out->cv = mean > 0.0 ? out->stddev / mean : 0.0;
+  out->min = mn;
+  out->max = mx;
+  out->total = total;
+  return EP_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,210 @@
+/*
+ * ep.h — C ABI of libep_b300: MoE expert-parallel token dispatch and combine
+ * on one NVIDIA B300 (sm_103a).
+ *
+ * The path (pages cited by title and section):
+ *   ep_route     top-k gating with softmax weights over fp32 router logits
+ *                (MoE sparse-communication article, intelliparadigm.com, §2.1
+ *                 Router listing: softmax over the logits, then topk)
+ *   ep_dispatch  group every (token, slot) copy by destination into one
+ *                contiguous rank-major buffer — "aggregate by target card"
+ *                (ThunderEP on consumer GPUs, bjdmk.com.cn, §2.1) with the
+ *                flat [rank0_data, rank1_data, ...] layout whose segments
+ *                start at running sums of the counts (NCCL EP article,
+ *                hotelren.com, §3.3) — fused with optional per-token dynamic
+ *                int8 compression (ThunderEP §2.3)
+ *   ep_combine   gate-weighted sum of each token's k expert outputs at its
+ *                source (ThunderEP §1.3 steps 3-4; §3.3 combine), fp32
+ *                accumulate in fixed slot order
+ * The R expert-parallel ranks are virtual: expert e belongs to rank e/(E/R)
+ * (MoE communication-wall explainer, juhe.plus, "64 experts on 8 GPUs"), and
+ * rank r's send block is payload rows [rank_off[r], rank_off[r+1]).
+ *
+ * Conventions for every call:
+ *   - All array pointers are caller-owned device memory unless stated; the
+ *     library allocates nothing and keeps no state between calls apart from
+ *     per-device launch settings. Scratch comes from a caller-provided
+ *     workspace sized by ep_workspace_size().
+ *   - Calls are asynchronous on the given stream (0 = legacy default stream)
+ *     and never synchronise it, except ep_get_error().
+ *   - Errors are returned, never raised by exit/abort (the NCCL EP article,
+ *     §4.2-4.3, on returning errors instead of hanging or exiting). Argument
+ *     checks run on the host before any launch: a call that returns
+ *     EP_ERR_INVALID_ARG or EP_ERR_WORKSPACE has enqueued nothing.
+ *   - Index inputs that come from the caller (topk_idx, slot_row) are checked
+ *     on the device too: an out-of-range or repeated entry is never used as an
+ *     address; it sets EP_ERR_DEVICE_INDEX in the workspace's status word,
+ *     which ep_get_error() reports.
+ *   - Alignment: float and bf16 arrays 16-byte aligned; int32 arrays 4-byte.
+ *   - Layouts are row-major and dense (no strides).
+ */
+#ifndef EP_B300_H_
+#define EP_B300_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  EP_OK = 0,
+  EP_ERR_INVALID_ARG = 1,  /* bad config, null or misaligned pointer      */
+  EP_ERR_WORKSPACE = 2,    /* workspace missing or smaller than required */
+  EP_ERR_CUDA = 3,         /* a CUDA runtime call or launch failed        */
+  EP_ERR_TIMEOUT = 4,      /* a bounded device-side wait gave up          */
+  EP_ERR_DEVICE_INDEX = 5  /* an index input was out of range or repeated */
+} ep_status_t;
+
+typedef enum {
+  EP_PAYLOAD_BF16 = 0, /* rows are the token's bf16 bytes, unchanged              */
+  EP_PAYLOAD_INT8 = 1  /* rows are the token's int8 code + one fp32 scale per row */
+} ep_payload_t;
+
+/*
+ * Problem statement (ThunderEP §1.3: T tokens, hidden size, E experts, top-k,
+ * N cards; juhe.plus all-to-all volume 2*T*k*H*b).
+ *   T                tokens in the batch, >= 0
+ *   H                hidden size, 16 <= H <= 16384, H % 16 == 0
+ *   E                experts, 1 <= E <= 1024
+ *   k                experts per token, 1 <= k <= min(E, 32)
+ *   R                virtual ranks, R >= 1, E % R == 0
+ *   capacity_factor  <= 0: dropless. > 0: each expert keeps at most
+ *                    cap = ceil(capacity_factor * T * k / E) copies (evaluated
+ *                    in double, in that order); further (token, slot) pairs
+ *                    are dropped in (token, slot) order and their weight is
+ *                    excluded from the combine (intelliparadigm §2.1 capacity
+ *                    factor, typical 1.0-1.25)
+ *   renormalize      0: w = full softmax probability of the chosen expert;
+ *                    1: the k chosen weights are rescaled to sum to one
+ *   payload          EP_PAYLOAD_BF16 or EP_PAYLOAD_INT8 for ep_dispatch
+ */
+typedef struct {
+  int32_t T, H, E, k, R;
+  float capacity_factor;
+  int32_t renormalize;
+  int32_t payload; /* ep_payload_t */
+} ep_config_t;
+
+/* Human-readable name of a status code (static storage). */
+const char* ep_status_string(ep_status_t s);
+
+/* Checks a config against the limits above (host only). */
+ep_status_t ep_config_check(const ep_config_t* cfg);
+
+/* Per-expert cap (T when dropless). Host only. */
+ep_status_t ep_capacity(const ep_config_t* cfg, int32_t* cap);
+
+/* Rows the dispatch buffers must hold: T*k dropless, else min(T*k, E*cap).
+ * Returns 0 for an invalid config. Host only. */
+int64_t ep_max_rows(const ep_config_t* cfg);
+
+/* Workspace bytes needed by ep_dispatch / ep_combine for this config. The
+ * size grows with T*k (a 4-byte rank per pair) plus E*ceil(T/tile) counters.
+ * Host only. */
+ep_status_t ep_workspace_size(const ep_config_t* cfg, size_t* bytes);
+
+/* Zero a freshly allocated workspace (its status word must start clear).
+ * Enqueued on `stream`. Needed once per allocation, not per call. */
+ep_status_t ep_workspace_init(void* ws, size_t ws_bytes, cudaStream_t stream);
+
+/*
+ * ep_route — top-k gating (intelliparadigm §2.1 Router; NCCL EP §3.4 step 1).
+ *   logits    [T, E] fp32 in   router scores (kept in fp32: the NCCL EP
+ *                              article, §6.3, warns that low-precision scores
+ *                              distort top-k)
+ *   topk_idx  [T, k] int32 out expert ids, slot j = j-th by (logit desc,
+ *                              expert id asc); ties go to the lower id
+ *   topk_w    [T, k] fp32 out  softmax weight of each chosen expert (see
+ *                              ep_config_t.renormalize); within 1e-6 relative
+ *                              of the exactly rounded value
+ * NaN/Inf logits are outside the contract (they are never used as addresses).
+ */
+ep_status_t ep_route(const ep_config_t* cfg, const float* logits, int32_t* topk_idx, float* topk_w,
+                     cudaStream_t stream);
+
+/*
+ * ep_dispatch — rank-major send layout plus its inverse (ThunderEP §2.1 and
+ * §2.3; NCCL EP §3.3 sendcounts/flat sendbuff).
+ *   x              [T, H] bf16 in     token hidden states
+ *   topk_idx       [T, k] int32 in    k distinct expert ids per token
+ *   payload        [max_rows, H] out  bf16 (EP_PAYLOAD_BF16) or int8
+ *                                     (EP_PAYLOAD_INT8); rows [0, N) are
+ *                                     written, N = T*k - dropped; row order is
+ *                                     (expert, token), so rank r's block is
+ *                                     rows [rank_off[r], rank_off[r+1])
+ *   scales         [max_rows] fp32 out one scale per row (int8 only; NULL in
+ *                                     bf16 mode): scale = amax/127.0f,
+ *                                     q = clamp(rint(x/scale), -127, 127)
+ *   row_slot       [max_rows] int32 out row -> t*k + j, rows [0, N)
+ *   slot_row       [T*k] int32 out    (t, j) -> row, or -1 if dropped
+ *   expert_counts  [E] int32 out      kept copies per expert
+ *   expert_raw     [E] int32 out      copies per expert before the cap (may be NULL)
+ *   expert_off     [E+1] int32 out    exclusive running sum of expert_counts
+ *   rank_off       [R+1] int32 out    rank_off[r] = expert_off[r*E/R] (the
+ *                                     send displacements; rank_off[R] = N)
+ *   n_dropped      [1] int32 out      pairs dropped by the cap
+ *   ws, ws_bytes   workspace from ep_workspace_size(), initialised once
+ * Counts and offsets stay on the device; copy rank_off back if the host needs N.
+ */
+ep_status_t ep_dispatch(const ep_config_t* cfg, const void* x, const int32_t* topk_idx, void* payload,
+                        float* scales, int32_t* row_slot, int32_t* slot_row, int32_t* expert_counts,
+                        int32_t* expert_raw, int32_t* expert_off, int32_t* rank_off, int32_t* n_dropped,
+                        void* ws, size_t ws_bytes, cudaStream_t stream);
+
+/*
+ * ep_combine — weighted top-k recombination (ThunderEP §1.3 steps 3-4).
+ *   expert_out   [max_rows, H] in  bf16 (out_payload = EP_PAYLOAD_BF16) or
+ *                                  int8 (EP_PAYLOAD_INT8) expert outputs,
+ *                                  row-aligned with the dispatch payload
+ *   out_scales   [max_rows] fp32   per-row scales for int8 rows, else NULL
+ *   slot_row     [T*k] int32 in    from ep_dispatch (-1 = dropped slot)
+ *   topk_w       [T, k] fp32 in    from ep_route
+ *   y            [T, H] bf16 out   y[t] = bf16_rne(sum over j = 0..k-1 in
+ *                                  order, slot not dropped, of
+ *                                  fmaf(w[t,j], v_j, acc)), acc starting at 0,
+ *                                  v_j = float(bf16) or (float)q * scale
+ *   ws, ws_bytes workspace (its status word records bad slot_row entries)
+ * A token whose k slots were all dropped gets y = 0.
+ */
+ep_status_t ep_combine(const ep_config_t* cfg, const void* expert_out, const float* out_scales,
+                       int32_t out_payload, const int32_t* slot_row, const float* topk_w, void* y,
+                       void* ws, size_t ws_bytes, cudaStream_t stream);
+
+/*
+ * ep_quantize_rows — the per-token int8 code applied to n rows of width H
+ * (ThunderEP §2.3), for an expert side that returns int8 outputs.
+ *   in      [n, H] bf16 in;  q [n, H] int8 out;  scales [n] fp32 out.
+ *   H % 16 == 0, 16 <= H <= 16384.
+ */
+ep_status_t ep_quantize_rows(const void* in, int64_t n, int32_t H, int8_t* q, float* scales,
+                             cudaStream_t stream);
+
+/*
+ * ep_get_error — synchronises `stream`, reads the workspace's status word,
+ * clears it, and returns EP_OK, EP_ERR_DEVICE_INDEX or EP_ERR_TIMEOUT (or
+ * EP_ERR_CUDA if the stream itself failed). The one call that blocks.
+ */
+ep_status_t ep_get_error(void* ws, size_t ws_bytes, cudaStream_t stream);
+
+/*
+ * Load statistics over per-expert counts already copied to the host
+ * (intelliparadigm §2.1: watch the spread of expert calls; coefficient of
+ * variation below 0.3 is the healthy range; NCCL EP §5.3 ncclEpStats_t idea).
+ */
+typedef struct {
+  double mean, stddev, cv; /* population standard deviation; cv = stddev/mean */
+  int32_t min, max;
+  int64_t total;
+} ep_load_stats_t;
+
+ep_status_t ep_load_stats(const int32_t* host_counts, int32_t E, ep_load_stats_t* out);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* EP_B300_H_ */

@@ -1,0 +1,320 @@
+"""GPU parity: the CUDA path through the C ABI against the CPU oracle.
+
+Every workload shape runs through the same entry points the bench times
+(ep_route -> ep_dispatch -> ep_combine on one stream). Where the oracle
+finishes in seconds the whole output is compared; at T=131072, H=8192 the
+routing and all layout metadata are compared in full and the payload and the
+combined rows on a sample. Tolerances are stated in tests/parity.py.
+"""
+import numpy as np
+import pytest
+import torch
+
+from parity import assert_combine_close, assert_weights_close, bf16_to_f32
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def ep():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA GPU")
+    from combine_warp_top_fp32_b300 import binding
+
+    return binding
+
+
+def _bits(t):
+    from combine_warp_top_fp32_b300.workloads import bf16_bits
+
+    return bf16_bits(t)
+
+
+def _run_path(ep, cfg, logits, x, expert_out):
+    buf = ep.EpBuffers.allocate(cfg)
+    buf.step(logits, x, expert_out)
+    torch.cuda.synchronize()
+    assert ep.ep_get_error(buf.ws) == ep.EP_OK
+    return buf
+
+
+def _check_layout(buf, lay, N):
+    np.testing.assert_array_equal(buf.expert_counts.cpu().numpy(), lay["expert_counts"])
+    np.testing.assert_array_equal(buf.expert_raw.cpu().numpy(), lay["expert_raw"])
+    np.testing.assert_array_equal(buf.expert_off.cpu().numpy(), lay["expert_off"])
+    np.testing.assert_array_equal(buf.rank_off.cpu().numpy(), lay["rank_off"])
+    assert int(buf.n_dropped.item()) == lay["n_dropped"]
+    np.testing.assert_array_equal(buf.slot_row.cpu().numpy(), lay["slot_row"])
+    np.testing.assert_array_equal(buf.row_slot[:N].cpu().numpy(), lay["row_slot"])
+
+
+def _full_parity(ep, orc, w, payload, renormalize=False, device_gen="cuda"):
+    from combine_warp_top_fp32_b300 import workloads
+
+    w = w.replace(renormalize=renormalize)
+    cfg = ep.config_from_workload(w, payload=payload)
+    d = workloads.generate(w, device=device_gen)
+    logits, x, eo = (d[n].cuda() for n in ("logits", "x", "expert_out"))
+    buf = _run_path(ep, cfg, logits, x, eo)
+
+    logits_h = logits.cpu().numpy()
+    x_bits = _bits(x)
+    eo_bits = _bits(eo)
+    # route: indices bit-exact, weights within 1e-6 relative
+    idx, wts = orc.route(logits_h, w.k, renormalize)
+    np.testing.assert_array_equal(buf.topk_idx.cpu().numpy(), idx)
+    worst_w = assert_weights_close(buf.topk_w.cpu().numpy(), wts)
+    # counts, offsets, permutation: bit-exact
+    lay = orc.layout(idx, w.E, w.R, w.capacity_factor)
+    N = lay["N"]
+    _check_layout(buf, lay, N)
+    # payload: bit-exact bytes (bf16) or codes + scales (int8)
+    int8 = payload == ep.EP_PAYLOAD_INT8
+    pl, sc = orc.payload(x_bits, lay["row_slot"], w.k, int8)
+    if int8:
+        np.testing.assert_array_equal(buf.payload[:N].cpu().numpy(), pl)
+        np.testing.assert_array_equal(buf.scales[:N].cpu().numpy(), sc)
+    else:
+        np.testing.assert_array_equal(_bits(buf.payload[:N]), pl)
+    # combine through the whole path
+    y_orc = orc.combine(eo_bits, None, lay["slot_row"], wts, w.T, w.k)
+    eo_f = lambda rows: bf16_to_f32(eo_bits[rows]).astype(np.float64)
+    stats = assert_combine_close(_bits(buf.y), y_orc, wts, lay["slot_row"], eo_f, w.k)
+    # combine alone on identical inputs: bit-exact
+    slot_row_d = torch.from_numpy(lay["slot_row"]).cuda()
+    w_d = torch.from_numpy(wts).cuda()
+    y2 = torch.empty_like(buf.y)
+    ep.ep_combine(cfg, eo, None, ep.EP_PAYLOAD_BF16, slot_row_d, w_d, y2, buf.ws)
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(_bits(y2), y_orc)
+    return dict(N=N, dropped=lay["n_dropped"], worst_w_rel=worst_w, **stats)
+
+
+CASES = [("tiny", 0), ("decode-latency", 1), ("prefill-mid", 0), ("prefill-mid", 1), ("capacity", 1)]
+
+
+@pytest.mark.parametrize("name,payload", CASES)
+def test_workload_parity(ep, orc, name, payload):
+    from combine_warp_top_fp32_b300 import workloads
+
+    info = _full_parity(ep, orc, workloads.WORKLOADS[name], payload)
+    print(name, payload, info)
+    if name == "capacity":
+        assert info["dropped"] > 0  # the cap binds on this skewed workload
+
+
+@pytest.mark.parametrize("name", ["tiny", "prefill-mid"])
+def test_workload_parity_renormalized(ep, orc, name):
+    from combine_warp_top_fp32_b300 import workloads
+
+    _full_parity(ep, orc, workloads.WORKLOADS[name], 0, renormalize=True)
+
+
+@pytest.mark.parametrize("payload", [0, 1])
+def test_large_parity_sampled(ep, orc, payload):
+    """T=131072, H=8192, E=256, k=8 at full size, in the bench's launch configuration.
+    Routing and all layout metadata compared in full; payload rows and combined
+    tokens on a sample (the oracle computes them one by one)."""
+    from combine_warp_top_fp32_b300 import workloads
+
+    w = workloads.WORKLOADS["large"]
+    cfg = ep.config_from_workload(w, payload=payload)
+    d = workloads.generate(w, device="cuda")
+    logits, x, eo = d["logits"], d["x"], d["expert_out"]
+    buf = _run_path(ep, cfg, logits, x, eo)
+    idx, wts = orc.route(logits.cpu().numpy(), w.k)
+    np.testing.assert_array_equal(buf.topk_idx.cpu().numpy(), idx)
+    assert_weights_close(buf.topk_w.cpu().numpy(), wts)
+    lay = orc.layout(idx, w.E, w.R, w.capacity_factor)
+    N = lay["N"]
+    assert N == w.T * w.k
+    _check_layout(buf, lay, N)
+
+    rng = np.random.default_rng(44)
+    roff = lay["rank_off"]
+    edge_rows = np.concatenate([roff[:-1], np.maximum(roff[1:] - 1, 0), [N - 1]])
+    rows = np.unique(np.concatenate([rng.integers(0, N, 4096), edge_rows]))
+    x_bits = _bits(x)
+    int8 = payload == ep.EP_PAYLOAD_INT8
+    pl, sc = orc.payload(x_bits, lay["row_slot"][rows], w.k, int8)
+    rows_d = torch.from_numpy(rows).long().cuda()
+    got = buf.payload.index_select(0, rows_d)
+    if int8:
+        np.testing.assert_array_equal(got.cpu().numpy(), pl)
+        np.testing.assert_array_equal(buf.scales.index_select(0, rows_d).cpu().numpy(), sc)
+    else:
+        np.testing.assert_array_equal(_bits(got), pl)
+    del x_bits
+
+    toks = np.unique(np.concatenate([rng.integers(0, w.T, 1024), [0, w.T - 1]]))
+    sr = lay["slot_row"].reshape(w.T, w.k)[toks]
+    need = np.unique(sr[sr >= 0])
+    eo_sub = _bits(eo.index_select(0, torch.from_numpy(need).long().cuda()))
+    remap = np.full(N, -1, np.int64)
+    remap[need] = np.arange(need.size)
+    sr_sub = np.where(sr >= 0, remap[np.maximum(sr, 0)], -1).astype(np.int32)
+    w_sub = wts[toks]
+    y_orc = orc.combine(eo_sub, None, sr_sub, w_sub, toks.size, w.k)
+    y_gpu = _bits(buf.y.index_select(0, torch.from_numpy(toks).long().cuda()))
+    eo_f = lambda r: bf16_to_f32(eo_sub[r]).astype(np.float64)
+    assert_combine_close(y_gpu, y_orc, w_sub, sr_sub, eo_f, w.k)
+
+
+# ----------------------------------------------------------------------------
+# edge cases: ragged tiles, extreme sizes, degenerate routing
+# ----------------------------------------------------------------------------
+EDGE = [
+    # T, H, E, k, R, cf, payload, renorm, note
+    (1, 16, 1, 1, 1, 0.0, 0, 0, "one token, one expert, minimum H"),
+    (1000, 64, 8, 2, 2, 0.0, 1, 0, "ragged last tile"),
+    (2500, 48, 6, 3, 3, 0.0, 0, 1, "E not a power of two, two ragged tiles"),
+    (777, 16384, 4, 2, 2, 0.0, 1, 0, "maximum H"),
+    (300, 32, 1024, 32, 8, 0.0, 1, 1, "maximum E and k"),
+    (513, 32, 160, 5, 160, 0.0, 0, 0, "E = R: one expert per rank, non-pow2 values per lane"),
+    (400, 64, 16, 16, 4, 0.0, 0, 0, "k = E: every expert"),
+    (3000, 128, 32, 4, 4, 0.25, 1, 0, "heavy capacity drops"),
+    (2048, 256, 64, 6, 8, 1.0, 0, 1, "capacity factor 1.0, bf16"),
+]
+
+
+@pytest.mark.parametrize("T,H,E,k,R,cf,payload,renorm,note", EDGE, ids=[e[-1] for e in EDGE])
+def test_edge_case_parity(ep, orc, T, H, E, k, R, cf, payload, renorm, note):
+    from combine_warp_top_fp32_b300 import workloads
+
+    w = workloads.Workload("edge", T=T, H=H, E=E, k=k, R=R, capacity_factor=cf, payloads=(payload,), seed=T + E,
+                           sigma_bias=1.0)
+    info = _full_parity(ep, orc, w, payload, renormalize=bool(renorm), device_gen="cpu")
+    if cf == 0.25:
+        assert info["dropped"] > 0
+
+
+def test_all_ties_pick_lowest_ids(ep, orc):
+    cfg = ep.make_config(64, 32, 16, 4, 4)
+    logits = torch.zeros(64, 16, device="cuda")
+    logits[::2] = -0.0  # -0 and +0 tie
+    buf = ep.EpBuffers.allocate(cfg)
+    buf.route(logits)
+    torch.cuda.synchronize()
+    assert np.all(buf.topk_idx.cpu().numpy() == np.arange(4))
+    np.testing.assert_allclose(buf.topk_w.cpu().numpy(), 1.0 / 16, rtol=1e-6)
+
+
+def test_empty_batch(ep):
+    cfg = ep.make_config(0, 64, 8, 2, 2, payload=ep.EP_PAYLOAD_INT8)
+    buf = ep.EpBuffers.allocate(cfg)
+    buf.expert_off.fill_(7)
+    buf.rank_off.fill_(7)
+    buf.n_dropped.fill_(7)
+    x = torch.empty(0, 64, dtype=torch.bfloat16, device="cuda")
+    buf.step(torch.empty(0, 8, device="cuda"), x, torch.empty(0, 64, dtype=torch.bfloat16, device="cuda"))
+    torch.cuda.synchronize()
+    assert buf.expert_off.cpu().tolist() == [0] * 9
+    assert buf.rank_off.cpu().tolist() == [0] * 3
+    assert buf.n_dropped.item() == 0
+    assert ep.ep_get_error(buf.ws) == ep.EP_OK
+
+
+def test_int8_return_path(ep, orc):
+    """Expert outputs coded per row (ep_quantize_rows) then combined as int8."""
+    from combine_warp_top_fp32_b300 import workloads
+
+    w = workloads.WORKLOADS["prefill-mid"]
+    cfg = ep.config_from_workload(w, payload=ep.EP_PAYLOAD_INT8)
+    d = workloads.generate(w, device="cuda")
+    rows = w.max_rows()
+    q = torch.empty(rows, w.H, dtype=torch.int8, device="cuda")
+    s = torch.empty(rows, dtype=torch.float32, device="cuda")
+    ep.ep_quantize_rows(d["expert_out"], q, s)
+    torch.cuda.synchronize()
+    q_o, s_o = orc.quantize_rows(_bits(d["expert_out"]))
+    np.testing.assert_array_equal(q.cpu().numpy(), q_o)
+    np.testing.assert_array_equal(s.cpu().numpy(), s_o)
+    idx, wts = orc.route(d["logits"].cpu().numpy(), w.k)
+    lay = orc.layout(idx, w.E, w.R, w.capacity_factor)
+    y_orc = orc.combine(q_o, s_o, lay["slot_row"], wts, w.T, w.k)
+    buf = ep.EpBuffers.allocate(cfg)
+    y = torch.empty(w.T, w.H, dtype=torch.bfloat16, device="cuda")
+    ep.ep_combine(cfg, q, s, ep.EP_PAYLOAD_INT8, torch.from_numpy(lay["slot_row"]).cuda(),
+                  torch.from_numpy(wts).cuda(), y, buf.ws)
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(_bits(y), y_orc)
+
+
+@pytest.mark.parametrize("payload", [0, 1])
+def test_identity_experts_round_trip(ep, payload):
+    """combine(dispatch(x)) with identity experts and renormalised weights gives x back."""
+    T, H, E, k, R = 2048, 512, 32, 4, 4
+    cfg = ep.make_config(T, H, E, k, R, renormalize=True, payload=payload)
+    g = torch.Generator(device="cuda").manual_seed(5)
+    logits = torch.randn(T, E, device="cuda", generator=g)
+    x = torch.randn(T, H, device="cuda", generator=g).to(torch.bfloat16)
+    buf = ep.EpBuffers.allocate(cfg)
+    buf.route(logits)
+    buf.dispatch(x)
+    buf.combine(buf.payload, buf.scales)
+    torch.cuda.synchronize()
+    xf = x.float().cpu().numpy().astype(np.float64)
+    yf = buf.y.float().cpu().numpy().astype(np.float64)
+    from parity import bf16_ulp
+
+    if payload == 0:
+        assert np.all(np.abs(yf - xf) <= bf16_ulp(xf))
+    else:
+        s_tok = np.zeros(T)
+        rs = buf.row_slot.cpu().numpy()
+        s_tok[rs // k] = buf.scales.cpu().numpy()
+        assert np.all(np.abs(yf - xf) <= (s_tok / 2)[:, None] * 1.0001 + bf16_ulp(xf))
+
+
+def test_deterministic_bytes(ep):
+    from combine_warp_top_fp32_b300 import workloads
+
+    w = workloads.WORKLOADS["prefill-mid"]
+    cfg = ep.config_from_workload(w, payload=ep.EP_PAYLOAD_INT8)
+    d = workloads.generate(w, device="cuda")
+    outs = []
+    for _ in range(2):
+        buf = _run_path(ep, cfg, d["logits"], d["x"], d["expert_out"])
+        outs.append([t.clone() for t in (buf.topk_idx, buf.topk_w, buf.payload, buf.scales, buf.slot_row, buf.y)])
+    for a, b in zip(*outs):
+        assert torch.equal(a, b)
+
+
+# ----------------------------------------------------------------------------
+# device-side index checks: bad inputs become a status code, never an access
+# ----------------------------------------------------------------------------
+def test_bad_expert_ids_are_reported(ep):
+    T, H, E, k, R = 100, 64, 8, 2, 2
+    cfg = ep.make_config(T, H, E, k, R)
+    buf = ep.EpBuffers.allocate(cfg)
+    idx = torch.stack([torch.arange(T) % E, (torch.arange(T) + 1) % E], 1).int().cuda()
+    idx[3, 1] = 8  # out of range
+    idx[7, 0] = -5  # negative
+    idx[9, 1] = idx[9, 0]  # repeated within a token
+    buf.topk_idx.copy_(idx)
+    x = torch.randn(T, H, device="cuda").to(torch.bfloat16)
+    buf.dispatch(x)
+    assert ep.ep_get_error(buf.ws) == ep.EP_ERR_DEVICE_INDEX
+    sr = buf.slot_row.cpu().numpy().reshape(T, k)
+    assert sr[3, 1] == -1 and sr[7, 0] == -1
+    N = int(buf.rank_off[-1].item())
+    assert np.all((sr == -1) | ((sr >= 0) & (sr < N)))
+    # the status word was cleared by the read
+    assert ep.ep_get_error(buf.ws) == ep.EP_OK
+
+
+def test_bad_slot_rows_are_reported(ep):
+    T, H, E, k, R = 16, 64, 4, 2, 2
+    cfg = ep.make_config(T, H, E, k, R)
+    buf = ep.EpBuffers.allocate(cfg)
+    eo = torch.ones(T * k, H, dtype=torch.bfloat16, device="cuda")
+    sr = torch.arange(T * k, dtype=torch.int32, device="cuda")
+    sr[5] = T * k  # one past the last row
+    sr[6] = -2
+    w = torch.full((T, k), 0.5, device="cuda")
+    y = torch.empty(T, H, dtype=torch.bfloat16, device="cuda")
+    ep.ep_combine(cfg, eo, None, ep.EP_PAYLOAD_BF16, sr, w, y, buf.ws)
+    assert ep.ep_get_error(buf.ws) == ep.EP_ERR_DEVICE_INDEX
+    yf = y.float().cpu().numpy()
+    assert np.all(yf[2] == 0.5) and np.all(yf[3] == 0.5)  # slots 5 and 6 skipped
+    assert np.all(yf[0] == 1.0)
