@@ -261,12 +261,13 @@ def cpu_model():
     return f"unknown (nproc={os.cpu_count()})"
 
 
-def workload_config(w, payload, n_rows):
+def workload_config(w, payload, n_rows, eager=False):
     return {"workload": w.name, "T": w.T, "H": w.H, "E": w.E, "k": w.k, "R": w.R,
             "capacity_factor": w.capacity_factor, "cap": w.capacity() if w.capacity_factor > 0 else None,
             "payload": payload, "expert_out": "bf16", "rows_dispatched": n_rows,
             "l2": "no flush: each step moves > 1 GB, far beyond the 126 MB L2",
-            "parallelism": "replicas (R virtual ranks per GPU)"}
+            "parallelism": "replicas (R virtual ranks per GPU)",
+            "launch": "eager" if eager else "cuda-graph replay per stage"}
 
 
 # ----------------------------------------------------------------------------
@@ -298,7 +299,33 @@ def run_gpu(args):
     torch.cuda.synchronize()
     assert ep.ep_get_error(buf.ws) == ep.EP_OK
     N = int(buf.rank_off[-1].item())
-    launches_per_step = 5 if w.T > 0 else 1
+    launches_per_step = 6 if w.T > 0 else 2  # route; count, scan, rows, scatter; combine
+
+    # The step's launches are captured once per stage as CUDA graphs (the
+    # library never synchronises or allocates, so its calls capture as they
+    # are); replaying them takes the host's per-call overhead off the GPU's
+    # critical path. Events between the three replays time each stage live.
+    stage_fns = {"route": lambda: buf.route(logits), "dispatch": lambda: buf.dispatch(x),
+                 "combine": lambda: buf.combine(eo)}
+    graphs = {}
+    if not args.eager:
+        side = torch.cuda.Stream()
+        side.wait_stream(stream)
+        with torch.cuda.stream(side):
+            for fn in stage_fns.values():
+                fn()
+        stream.wait_stream(side)
+        for name, fn in stage_fns.items():
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                fn()
+            graphs[name] = g
+        for _ in range(args.warmup):
+            for g in graphs.values():
+                g.replay()
+        torch.cuda.synchronize()
+        assert ep.ep_get_error(buf.ws) == ep.EP_OK
+    run = {n: (graphs[n].replay if graphs else stage_fns[n]) for n in stage_fns}
 
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
     sampler = ClockSampler(local)
@@ -308,14 +335,15 @@ def run_gpu(args):
     for i in range(args.steps):
         e = ev[i]
         e[0].record(stream)
-        buf.route(logits)
+        run["route"]()
         e[1].record(stream)
-        buf.dispatch(x)
+        run["dispatch"]()
         e[2].record(stream)
-        buf.combine(eo)
+        run["combine"]()
         e[3].record(stream)
     torch.cuda.synchronize()
     barrier()
+    assert ep.ep_get_error(buf.ws) == ep.EP_OK
     clocks = sampler.stop()
     total_ms = ev[0][0].elapsed_time(ev[-1][3])
     stage_ms = {
@@ -333,7 +361,7 @@ def run_gpu(args):
     step_gbs = nb["total"] / (ms_per_step / 1e3) / 1e9
     stage_gbs = {s: nb[s] / (stage_ms[s] / 1e3) / 1e9 for s in stage_ms}
     dominant = max(stage_ms, key=stage_ms.get)
-    kernel_names = {"route": "route_topk_kernel", "dispatch": "count+scan+scatter_kernel",
+    kernel_names = {"route": "route_topk_kernel", "dispatch": "count+scan+rows+scatter_kernel",
                     "combine": "combine_kernel<bf16>"}
     traffic = recorded_traffic(dominant, w.name, args.payload)
 
@@ -385,7 +413,7 @@ def run_gpu(args):
         line = {
             "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "fp32", "data": "synthetic", "config": workload_config(w, args.payload, N),
+            "vs_baseline": None, "dtype": "fp32", "data": "synthetic", "config": workload_config(w, args.payload, N, args.eager),
             "hbm": {"bytes_per_step": nb["total"], "gbs": step_gbs, "frac_of_8000": step_gbs / NOMINAL_HBM_GBS,
                     f"frac_of_{peak_src}": step_gbs / peak, "metadata_bytes_per_step": nb["metadata"]},
             "stages": {s: {"ms": stage_ms[s], "bytes": nb[s], "gbs": stage_gbs[s]} for s in stage_ms},
@@ -412,6 +440,7 @@ def parse_args(argv=None):
     ap.add_argument("--workload", default="capacity")
     ap.add_argument("--payload", choices=["int8", "bf16"], default=None)
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--eager", action="store_true", help="launch through the binding each step (no CUDA graphs)")
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-baseline-s", type=float, default=15.0)

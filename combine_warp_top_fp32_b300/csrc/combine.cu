@@ -25,18 +25,29 @@ __global__ void __launch_bounds__(1024) combine_kernel(const CombineArgs a) {
   __shared__ float w_s[2][32];
   __shared__ float sc_s[2][32];
   const int nchunk = a.H >> 3;
+  // threads j < k carry slot j's row, weight (and scale) one token ahead
+  auto load_slot = [&](int64_t t, int& row, float& w, float& sc) {
+    const int64_t s = t * a.k + threadIdx.x;
+    row = a.slot_row[s];
+    if (row < -1 || static_cast<int64_t>(row) >= a.max_rows) {
+      raise_status(a.status, kStatusBadIndex);
+      row = -1;
+    }
+    w = a.topk_w[s];
+    sc = 0.f;
+    if constexpr (INT8) sc = row >= 0 ? a.out_scales[row] : 0.f;
+  };
+  int row_c = -1;
+  float w_c = 0.f, sc_c = 0.f;
+  if (blockIdx.x < a.T && threadIdx.x < a.k) load_slot(blockIdx.x, row_c, w_c, sc_c);
   int buf = 0;
   for (int64_t t = blockIdx.x; t < a.T; t += gridDim.x) {
     if (threadIdx.x < a.k) {
-      const int64_t s = t * a.k + threadIdx.x;
-      int row = a.slot_row[s];
-      if (row < -1 || static_cast<int64_t>(row) >= a.max_rows) {
-        raise_status(a.status, kStatusBadIndex);
-        row = -1;
-      }
-      rows_s[buf][threadIdx.x] = row;
-      w_s[buf][threadIdx.x] = a.topk_w[s];
-      if constexpr (INT8) sc_s[buf][threadIdx.x] = row >= 0 ? a.out_scales[row] : 0.f;
+      rows_s[buf][threadIdx.x] = row_c;
+      w_s[buf][threadIdx.x] = w_c;
+      if constexpr (INT8) sc_s[buf][threadIdx.x] = sc_c;
+      const int64_t tn = t + gridDim.x;
+      if (tn < a.T) load_slot(tn, row_c, w_c, sc_c);
     }
     __syncthreads();
     for (int c = threadIdx.x; c < nchunk; c += blockDim.x) {

@@ -153,6 +153,9 @@ ep_status_t ep_dispatch(const ep_config_t* cfg, const void* x, const int32_t* to
   a.rank_off = rank_off;
   a.n_dropped = n_dropped;
   a.status = reinterpret_cast<uint32_t*>(w + L.status_off);
+  a.ticket = reinterpret_cast<uint32_t*>(w + L.ticket_off);
+  a.kept = reinterpret_cast<int32_t*>(w + L.kept_off);
+  a.dropped = reinterpret_cast<int32_t*>(w + L.drop_off);
   a.tile_counts = reinterpret_cast<int32_t*>(w + L.tile_counts_off);
   a.tile_base = reinterpret_cast<int32_t*>(w + L.tile_base_off);
   a.lrank = reinterpret_cast<int32_t*>(w + L.lrank_off);

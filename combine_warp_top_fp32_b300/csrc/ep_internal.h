@@ -9,32 +9,38 @@
 
 namespace ep {
 
-// Tokens per counting tile, a function of E alone so that the workspace size
-// query and the dispatch agree. The count kernel keeps two E x (tile/32)
-// word arrays in shared memory (bit masks and their prefix counts).
-inline int tile_tokens_for(int E) {
-  if (static_cast<int64_t>(E) * (1024 / 32) * 4 * 2 <= 96 * 1024) return 1024;
-  if (static_cast<int64_t>(E) * (512 / 32) * 4 * 2 <= 96 * 1024) return 512;
-  return 256;
+// Tokens per counting tile, a function of (T, E) alone so that the workspace
+// size query and the dispatch agree: a power of two in [32, 1024] giving about
+// 256 tiles (enough CTAs for 148 SMs), shrunk until the count kernel's two
+// E x (tile/32) word arrays (bit masks and their prefix counts) fit in 96 KB.
+inline int tile_tokens_for(int T, int E) {
+  int tile = 32;
+  while (tile < 1024 && static_cast<int64_t>(tile) * 256 < T) tile <<= 1;
+  while (tile > 32 && static_cast<int64_t>(E) * (tile / 32) * 4 * 2 > 96 * 1024) tile >>= 1;
+  return tile;
 }
 
 // Workspace layout (each region 256-byte aligned):
-//   [status word | tile_counts E x ntiles | tile_base E x ntiles | lrank T*k]
+//   [status word, scan ticket | kept E | dropped E | tile_counts E x ntiles |
+//    tile_base E x ntiles | lrank T*k]
 struct WsLayout {
   int tile;
   int ntiles;
-  size_t status_off, tile_counts_off, tile_base_off, lrank_off, total;
+  size_t status_off, ticket_off, kept_off, drop_off, tile_counts_off, tile_base_off, lrank_off, total;
 };
 
 inline size_t align256(size_t v) { return (v + 255) & ~static_cast<size_t>(255); }
 
 inline WsLayout ws_layout(int T, int E, int k) {
   WsLayout L;
-  L.tile = tile_tokens_for(E);
+  L.tile = tile_tokens_for(T, E);
   L.ntiles = (T + L.tile - 1) / L.tile;
   const size_t counters = static_cast<size_t>(E) * static_cast<size_t>(L.ntiles) * sizeof(int32_t);
   L.status_off = 0;
-  L.tile_counts_off = 256;
+  L.ticket_off = 4;
+  L.kept_off = 256;
+  L.drop_off = L.kept_off + align256(static_cast<size_t>(E) * sizeof(int32_t));
+  L.tile_counts_off = L.drop_off + align256(static_cast<size_t>(E) * sizeof(int32_t));
   L.tile_base_off = L.tile_counts_off + align256(counters);
   L.lrank_off = L.tile_base_off + align256(counters);
   L.total = L.lrank_off + align256(static_cast<size_t>(T) * static_cast<size_t>(k) * sizeof(int32_t));
@@ -53,7 +59,8 @@ struct DispatchArgs {
   int32_t *row_slot, *slot_row, *expert_counts, *expert_raw, *expert_off, *rank_off, *n_dropped;
   // workspace regions
   uint32_t* status;
-  int32_t *tile_counts, *tile_base, *lrank;
+  uint32_t* ticket;
+  int32_t *kept, *dropped, *tile_counts, *tile_base, *lrank;
   int tile, ntiles;
 };
 

@@ -11,8 +11,10 @@
 //     L == 32 and E % 128 == 0), each lane holding VPL = ceil(E/L) values;
 //   - each value becomes a 64-bit key (order-preserving float bits << 32 |
 //     ~expert id), so one unsigned max picks (logit desc, id asc) exactly;
-//   - k rounds of: lane-local max, butterfly max over the group with
-//     __shfl_xor_sync, the owner clears the winning key; lane j keeps slot j;
+//   - k rounds of: lane-local max, group max, the owner clears the winning
+//     key; lane j keeps slot j. With one token per warp (E >= 32) the group
+//     max is two redux.sync reductions (value max, then lowest id holding
+//     it); with several tokens per warp it is a __shfl_xor_sync butterfly;
 //   - softmax denominator: exp(l - l_max) with the subtraction's rounding
 //     error carried into the exponential, summed with compensated (Neumaier /
 //     TwoSum) arithmetic, so the weight stays within 1e-6 of the exact value.
@@ -129,20 +131,59 @@ __global__ void __launch_bounds__(256) route_topk_kernel(const float* __restrict
     int my_e = 0;
     float my_v = 0.f;
     float l_max = 0.f;
-    for (int r = 0; r < k; ++r) {
-      uint64_t best = key[0];
+    if (L == 32) {
+      // One token per warp: two single-instruction warp reductions per round.
+      // redux.sync max over the order-preserving value bits finds the largest
+      // logit, redux.sync min over the ids of the lanes holding it breaks the
+      // tie toward the lower expert id. Within a lane the ids grow with i, so
+      // a strict '>' keeps the lowest id among the lane's equal values.
+      uint32_t ob[VPL];
 #pragma unroll
-      for (int i = 1; i < VPL; ++i) best = umax64(best, key[i]);
-      for (int o = L >> 1; o > 0; o >>= 1) best = umax64(best, __shfl_xor_sync(0xffffffffu, best, o));
-      const float v = key_value(best);
-      if (r == 0) l_max = v;
-      if (sub == r) {
-        my_e = key_expert(best);
-        my_v = v;
+      for (int i = 0; i < VPL; ++i) ob[i] = static_cast<uint32_t>(key[i] >> 32);
+      for (int r = 0; r < k; ++r) {
+        uint32_t bv = ob[0];
+        int bi = 0;
+#pragma unroll
+        for (int i = 1; i < VPL; ++i)
+          if (ob[i] > bv) {
+            bv = ob[i];
+            bi = i;
+          }
+        const uint32_t gmax = __reduce_max_sync(0xffffffffu, bv);
+        uint32_t my_id = 0xffffffffu;
+#pragma unroll
+        for (int i = 0; i < VPL; ++i)
+          if (i == bi) my_id = 0xffffffffu - static_cast<uint32_t>(key[i]);
+        const uint32_t cand = (bv == gmax) ? my_id : 0xffffffffu;
+        const uint32_t win = __reduce_min_sync(0xffffffffu, cand);
+        const float v = key_value(static_cast<uint64_t>(gmax) << 32);
+        if (r == 0) l_max = v;
+        if (sub == r) {
+          my_e = static_cast<int>(win);
+          my_v = v;
+        }
+        if (cand == win) {
+#pragma unroll
+          for (int i = 0; i < VPL; ++i)
+            if (i == bi) ob[i] = 0u;  // 0 is below every real value
+        }
       }
+    } else {
+      for (int r = 0; r < k; ++r) {
+        uint64_t best = key[0];
 #pragma unroll
-      for (int i = 0; i < VPL; ++i)
-        if (key[i] == best) key[i] = 0ull;
+        for (int i = 1; i < VPL; ++i) best = umax64(best, key[i]);
+        for (int o = L >> 1; o > 0; o >>= 1) best = umax64(best, __shfl_xor_sync(0xffffffffu, best, o));
+        const float v = key_value(best);
+        if (r == 0) l_max = v;
+        if (sub == r) {
+          my_e = key_expert(best);
+          my_v = v;
+        }
+#pragma unroll
+        for (int i = 0; i < VPL; ++i)
+          if (key[i] == best) key[i] = 0ull;
+      }
     }
 
     // softmax denominator: all E experts, or the k chosen when renormalising
