@@ -31,7 +31,7 @@ EP_PAYLOAD_INT8 = 1
 EXPORTS = (
     "ep_status_string", "ep_config_check", "ep_capacity", "ep_max_rows", "ep_workspace_size",
     "ep_workspace_init", "ep_route", "ep_dispatch", "ep_combine", "ep_quantize_rows", "ep_get_error",
-    "ep_load_stats",
+    "ep_load_stats", "ep_dispatch_static",
 )
 
 
@@ -77,6 +77,7 @@ def _load():
     lib.ep_quantize_rows.argtypes = [P, I64, I32, P, P, P]
     lib.ep_get_error.argtypes = [P, SZ, P]
     lib.ep_load_stats.argtypes = [P, I32, ctypes.POINTER(ep_load_stats_t)]
+    lib.ep_dispatch_static.argtypes = [CFG, P, P, P, P, P, P, P, P, P, P, P, P]
     for name in EXPORTS:
         if name not in ("ep_status_string", "ep_max_rows"):
             getattr(lib, name).restype = ctypes.c_int

@@ -156,6 +156,42 @@ ep_status_t ep_dispatch(const ep_config_t* cfg, const void* x, const int32_t* to
                         void* ws, size_t ws_bytes, cudaStream_t stream);
 
 /*
+ * ep_dispatch_static — ep_dispatch for callers that cannot allocate device
+ * memory. The pages have no counterpart to this call: it exists only for
+ * this library's users.
+ *
+ * Some callers cannot provide the workspace ep_dispatch needs: a plugin or
+ * custom-op host that passes an operator only its inputs and outputs and
+ * forbids allocation inside the enqueue call, a runtime that plans every
+ * device allocation ahead of time, or a latency-critical path that cannot
+ * afford cudaMalloc's implicit synchronisation. This call takes the same
+ * arguments as ep_dispatch minus the workspace, runs the same kernels, and
+ * keeps its scratch in a fixed device array of EP_STATIC_SCRATCH_BYTES inside
+ * the library, which every GPU that loads the library holds until exit. It
+ * calls no cudaMalloc, cudaFree or other allocating routine.
+ *   - Limit: a problem whose ep_workspace_size() exceeds
+ *     EP_STATIC_SCRATCH_BYTES is refused with EP_ERR_WORKSPACE before
+ *     anything is enqueued (the scratch is about 4*T*k + 8*E*ceil(T/tile)
+ *     bytes plus 2 KB: T=131072, k=8, E=256 needs about 4.6 MB).
+ *   - The first call on each device looks up the array's device address
+ *     (cudaGetSymbolAddress, with that device current); make that first call
+ *     before any stream capture starts.
+ *   - All calls share the one array and each call starts by clearing the part
+ *     that must begin at zero. Calls whose work overlaps on the GPU (other
+ *     streams, other host threads on the same device) race on it: serialise
+ *     them.
+ *   - Device-side index checks still guard every access, but their status
+ *     word lives in the shared array, so ep_get_error cannot report them;
+ *     diagnose bad indices with ep_dispatch and a workspace.
+ */
+#define EP_STATIC_SCRATCH_BYTES (8u * 1024u * 1024u)
+
+ep_status_t ep_dispatch_static(const ep_config_t* cfg, const void* x, const int32_t* topk_idx, void* payload,
+                               float* scales, int32_t* row_slot, int32_t* slot_row, int32_t* expert_counts,
+                               int32_t* expert_raw, int32_t* expert_off, int32_t* rank_off, int32_t* n_dropped,
+                               cudaStream_t stream);
+
+/*
  * ep_combine — weighted top-k recombination (ThunderEP §1.3 steps 3-4).
  *   expert_out   [max_rows, H] in  bf16 (out_payload = EP_PAYLOAD_BF16) or
  *                                  int8 (EP_PAYLOAD_INT8) expert outputs,
