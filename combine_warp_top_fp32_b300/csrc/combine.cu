@@ -10,109 +10,189 @@
 //   y[t,h] = bf16 round-to-nearest-even(acc)
 // The fixed slot order and the explicit fma make the result reproducible.
 //
-// Design: grid-stride over tokens, one CTA per token in flight, 8 elements
-// (one 16-byte bf16 load or one 8-byte int8 load) per thread and slot. The k
-// row loads of a thread are issued back to back (up to 8 in flight) before
-// any arithmetic, so each thread keeps up to 128 bytes of reads outstanding.
+// Design: one warp per token in flight, no block-level synchronisation.
+//   - lanes j < k read slot j's row, weight (and int8 scale) one token ahead;
+//   - a ballot drops the dropped slots and the kept ones are gathered, in
+//     slot order, into registers of every lane (row address, weight, scale),
+//     so a token with few kept slots costs only their loads;
+//   - the row is walked in 16-byte chunks per lane (8 bf16 or 16 int8
+//     elements); the loads of all kept slots for several chunks are issued
+//     back to back before any arithmetic, 16 per lane in flight whatever the
+//     number of kept slots (2 slots x 8 chunks, 4 x 4 or 8 x 2);
+//   - more than 8 kept slots (k > 8) are taken in groups of 8 in slot order,
+//     with the accumulators carried across groups, so the order of the fmas is
+//     the same in every case.
 #include "ep_internal.h"
 
 namespace ep {
 namespace {
 
+constexpr unsigned kFull = 0xffffffffu;
+
+// Bytes of one 16-byte chunk: 8 bf16 or 16 int8 elements.
 template <bool INT8>
-__global__ void __launch_bounds__(1024) combine_kernel(const CombineArgs a) {
-  __shared__ int32_t rows_s[2][32];
-  __shared__ float w_s[2][32];
-  __shared__ float sc_s[2][32];
-  const int nchunk = a.H >> 3;
-  // threads j < k carry slot j's row, weight (and scale) one token ahead
+struct Chunk {
+  static constexpr int kElems = INT8 ? 16 : 8;
+};
+
+// acc[0..EL) += w * v for one 16-byte chunk of a kept row, in element order.
+template <bool INT8>
+__device__ __forceinline__ void fma_chunk(float* acc, uint4 v, float w, float sc) {
+  if constexpr (INT8) {
+    const uint32_t u[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+#pragma unroll
+      for (int i = 0; i < 4; ++i) acc[4 * q + i] = __fmaf_rn(w, __fmul_rn(i8_at(u[q], i), sc), acc[4 * q + i]);
+  } else {
+    acc[0] = __fmaf_rn(w, bf16_lo(v.x), acc[0]);
+    acc[1] = __fmaf_rn(w, bf16_hi(v.x), acc[1]);
+    acc[2] = __fmaf_rn(w, bf16_lo(v.y), acc[2]);
+    acc[3] = __fmaf_rn(w, bf16_hi(v.y), acc[3]);
+    acc[4] = __fmaf_rn(w, bf16_lo(v.z), acc[4]);
+    acc[5] = __fmaf_rn(w, bf16_hi(v.z), acc[5]);
+    acc[6] = __fmaf_rn(w, bf16_lo(v.w), acc[6]);
+    acc[7] = __fmaf_rn(w, bf16_hi(v.w), acc[7]);
+  }
+}
+
+// Round EL fp32 accumulators to bf16 (RNE) and store them at y (16-byte aligned).
+template <int EL>
+__device__ __forceinline__ void store_bf16(char* y, const float* acc) {
+#pragma unroll
+  for (int s = 0; s < EL / 8; ++s) {
+    uint4 o;
+    o.x = pack_bf16x2_rn(acc[8 * s + 0], acc[8 * s + 1]);
+    o.y = pack_bf16x2_rn(acc[8 * s + 2], acc[8 * s + 3]);
+    o.z = pack_bf16x2_rn(acc[8 * s + 4], acc[8 * s + 5]);
+    o.w = pack_bf16x2_rn(acc[8 * s + 6], acc[8 * s + 7]);
+    st_v4(y + 16 * s, o);
+  }
+}
+
+// Gathers the next (up to) 8 kept slots of `mask` (lowest slot first) from the
+// lanes that hold them into registers of every lane; returns how many.
+template <bool INT8>
+__device__ __forceinline__ int gather_group(unsigned& mask, int row, float w, float sc, const char* base,
+                                            int64_t row_bytes, const char* (&p)[8], float (&wv)[8],
+                                            float (&sv)[8]) {
+  int n = 0;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const int src = mask ? __ffs(mask) - 1 : 0;  // uniform across the warp
+    const int r = __shfl_sync(kFull, row, src);
+    wv[i] = __shfl_sync(kFull, w, src);
+    if constexpr (INT8) sv[i] = __shfl_sync(kFull, sc, src);
+    p[i] = base + static_cast<int64_t>(r < 0 ? 0 : r) * row_bytes;
+    if (mask) ++n;
+    mask &= mask - 1u;
+  }
+  return n;
+}
+
+// One token's chunks with at most NS kept slots (gathered in p/wv/sv): UNR
+// chunks per lane per pass, all NS*UNR loads issued before any arithmetic.
+template <bool INT8, int NS, int UNR>
+__device__ __forceinline__ void combine_token(int nk, int nchunk, int lane, const char* const (&p)[8],
+                                              const float (&wv)[8], const float (&sv)[8], char* yrow) {
+  constexpr int EL = Chunk<INT8>::kElems;
+  for (int c0 = lane; c0 < nchunk; c0 += 32 * UNR) {
+    uint4 v[UNR][NS];
+#pragma unroll
+    for (int u = 0; u < UNR; ++u) {
+      const int c = c0 + 32 * u;
+#pragma unroll
+      for (int i = 0; i < NS; ++i)
+        v[u][i] = (i < nk && c < nchunk) ? ld_stream_v4(p[i] + 16 * static_cast<int64_t>(c)) : make_uint4(0, 0, 0, 0);
+    }
+#pragma unroll
+    for (int u = 0; u < UNR; ++u) {
+      const int c = c0 + 32 * u;
+      float acc[EL];
+#pragma unroll
+      for (int e = 0; e < EL; ++e) acc[e] = 0.f;
+#pragma unroll
+      for (int i = 0; i < NS; ++i)
+        if (i < nk) fma_chunk<INT8>(acc, v[u][i], wv[i], sv[i]);
+      if (c < nchunk) store_bf16<EL>(yrow + 2 * static_cast<int64_t>(c) * EL, acc);
+    }
+  }
+}
+
+// LOADS = 16-byte loads in flight per lane: a token with few kept slots walks
+// more chunks per pass, so the bytes in flight do not shrink with drops.
+template <bool INT8, int LOADS>
+__global__ void __launch_bounds__(256) combine_kernel(const CombineArgs a) {
+  constexpr int EL = Chunk<INT8>::kElems;
+  const int lane = threadIdx.x & 31;
+  const int64_t warp0 = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
+  const int nchunk = a.H / EL;
+  const int64_t row_bytes = INT8 ? a.H : 2 * static_cast<int64_t>(a.H);
+  const char* base = static_cast<const char*>(a.expert_out);
+
+  // lane j < k: slot j of token t (row, weight, scale); -1 / 0 elsewhere
   auto load_slot = [&](int64_t t, int& row, float& w, float& sc) {
-    const int64_t s = t * a.k + threadIdx.x;
-    row = a.slot_row[s];
-    if (row < -1 || static_cast<int64_t>(row) >= a.max_rows) {
-      raise_status(a.status, kStatusBadIndex);
-      row = -1;
-    }
-    w = a.topk_w[s];
+    row = -1;
+    w = 0.f;
     sc = 0.f;
-    if constexpr (INT8) sc = row >= 0 ? a.out_scales[row] : 0.f;
-  };
-  int row_c = -1;
-  float w_c = 0.f, sc_c = 0.f;
-  if (blockIdx.x < a.T && threadIdx.x < a.k) load_slot(blockIdx.x, row_c, w_c, sc_c);
-  int buf = 0;
-  for (int64_t t = blockIdx.x; t < a.T; t += gridDim.x) {
-    if (threadIdx.x < a.k) {
-      rows_s[buf][threadIdx.x] = row_c;
-      w_s[buf][threadIdx.x] = w_c;
-      if constexpr (INT8) sc_s[buf][threadIdx.x] = sc_c;
-      const int64_t tn = t + gridDim.x;
-      if (tn < a.T) load_slot(tn, row_c, w_c, sc_c);
+    if (t < a.T && lane < a.k) {
+      const int64_t s = t * a.k + lane;
+      row = a.slot_row[s];
+      if (row < -1 || static_cast<int64_t>(row) >= a.max_rows) {
+        raise_status(a.status, kStatusBadIndex);
+        row = -1;
+      }
+      w = a.topk_w[s];
+      if constexpr (INT8) sc = row >= 0 ? a.out_scales[row] : 0.f;
     }
-    __syncthreads();
-    for (int c = threadIdx.x; c < nchunk; c += blockDim.x) {
-      float acc[8];
+  };
+
+  int row_n, row;
+  float w_n, sc_n, w, sc;
+  load_slot(warp0, row_n, w_n, sc_n);
+  for (int64_t t = warp0; t < a.T; t += nwarps) {
+    row = row_n;
+    w = w_n;
+    sc = sc_n;
+    load_slot(t + nwarps, row_n, w_n, sc_n);  // the next token's slots, one token ahead
+
+    const unsigned kept = __ballot_sync(kFull, row >= 0);
+    const int nk = __popc(kept);
+    char* yrow = static_cast<char*>(a.y) + t * 2 * static_cast<int64_t>(a.H);
+    const char* p[8];
+    float wv[8], sv[8];
+    if (nk <= 8) {
+      unsigned m = kept;
+      gather_group<INT8>(m, row, w, sc, base, row_bytes, p, wv, sv);
+      if (nk <= 2)
+        combine_token<INT8, 2, LOADS / 2>(nk, nchunk, lane, p, wv, sv, yrow);
+      else if (nk <= 4)
+        combine_token<INT8, 4, LOADS / 4>(nk, nchunk, lane, p, wv, sv, yrow);
+      else
+        combine_token<INT8, 8, LOADS / 8>(nk, nchunk, lane, p, wv, sv, yrow);
+    } else {
+      // k > 8 with more than 8 kept slots: groups of 8 per chunk, slot order.
+      // The loop bound is warp-uniform: the gathers shuffle across all lanes.
+      for (int c0 = 0; c0 < nchunk; c0 += 32) {
+        const int c = c0 + lane;
+        float acc[EL];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) acc[i] = 0.f;
-      for (int j0 = 0; j0 < a.k; j0 += 8) {
-        const int nj = min(8, a.k - j0);
-        if constexpr (INT8) {
-          uint2 v[8];
-#pragma unroll
-          for (int jj = 0; jj < 8; ++jj) {
-            v[jj] = make_uint2(0, 0);
-            const int row = jj < nj ? rows_s[buf][j0 + jj] : -1;
-            if (row >= 0) v[jj] = ld_stream_v2(static_cast<const int8_t*>(a.expert_out) +
-                                               static_cast<int64_t>(row) * a.H + 8 * c);
-          }
-#pragma unroll
-          for (int jj = 0; jj < 8; ++jj) {
-            const int row = jj < nj ? rows_s[buf][j0 + jj] : -1;
-            if (row >= 0) {
-              const float w = w_s[buf][j0 + jj];
-              const float sc = sc_s[buf][j0 + jj];
-#pragma unroll
-              for (int i = 0; i < 4; ++i) {
-                acc[i] = __fmaf_rn(w, __fmul_rn(i8_at(v[jj].x, i), sc), acc[i]);
-                acc[4 + i] = __fmaf_rn(w, __fmul_rn(i8_at(v[jj].y, i), sc), acc[4 + i]);
-              }
-            }
-          }
-        } else {
+        for (int e = 0; e < EL; ++e) acc[e] = 0.f;
+        unsigned m = kept;
+        while (m) {
+          const int n = gather_group<INT8>(m, row, w, sc, base, row_bytes, p, wv, sv);
           uint4 v[8];
 #pragma unroll
-          for (int jj = 0; jj < 8; ++jj) {
-            v[jj] = make_uint4(0, 0, 0, 0);
-            const int row = jj < nj ? rows_s[buf][j0 + jj] : -1;
-            if (row >= 0)
-              v[jj] = ld_stream_v4(static_cast<const char*>(a.expert_out) +
-                                   (static_cast<int64_t>(row) * a.H + 8 * c) * 2);
-          }
+          for (int i = 0; i < 8; ++i)
+            v[i] = (i < n && c < nchunk) ? ld_stream_v4(p[i] + 16 * static_cast<int64_t>(c)) : make_uint4(0, 0, 0, 0);
 #pragma unroll
-          for (int jj = 0; jj < 8; ++jj) {
-            const int row = jj < nj ? rows_s[buf][j0 + jj] : -1;
-            if (row >= 0) {
-              const float w = w_s[buf][j0 + jj];
-              acc[0] = __fmaf_rn(w, bf16_lo(v[jj].x), acc[0]);
-              acc[1] = __fmaf_rn(w, bf16_hi(v[jj].x), acc[1]);
-              acc[2] = __fmaf_rn(w, bf16_lo(v[jj].y), acc[2]);
-              acc[3] = __fmaf_rn(w, bf16_hi(v[jj].y), acc[3]);
-              acc[4] = __fmaf_rn(w, bf16_lo(v[jj].z), acc[4]);
-              acc[5] = __fmaf_rn(w, bf16_hi(v[jj].z), acc[5]);
-              acc[6] = __fmaf_rn(w, bf16_lo(v[jj].w), acc[6]);
-              acc[7] = __fmaf_rn(w, bf16_hi(v[jj].w), acc[7]);
-            }
-          }
+          for (int i = 0; i < 8; ++i)
+            if (i < n) fma_chunk<INT8>(acc, v[i], wv[i], sv[i]);
         }
+        if (c < nchunk) store_bf16<EL>(yrow + 2 * static_cast<int64_t>(c) * EL, acc);
       }
-      uint4 out;
-      out.x = pack_bf16x2_rn(acc[0], acc[1]);
-      out.y = pack_bf16x2_rn(acc[2], acc[3]);
-      out.z = pack_bf16x2_rn(acc[4], acc[5]);
-      out.w = pack_bf16x2_rn(acc[6], acc[7]);
-      st_v4(static_cast<char*>(a.y) + (t * a.H + 8 * c) * 2, out);
     }
-    buf ^= 1;
   }
 }
 
@@ -131,41 +211,53 @@ __global__ void __launch_bounds__(1024) quantize_rows_kernel(const void* __restr
       a0 = ld_stream_v4(p);
       a1 = ld_stream_v4(p + 16);
     }
-    float m = on ? fmaxf(absmax_bf16x8(a0), absmax_bf16x8(a1)) : 0.f;
+    float m = on ? absmax_bf16x16(a0, a1) : 0.f;
     m = warp_max(m);
     if (lane == 0) amax_s[buf][warp] = m;
     __syncthreads();
     float am = amax_s[buf][0];
     for (int i = 1; i < nw; ++i) am = fmaxf(am, amax_s[buf][i]);
     const float scale = __fdiv_rn(am, 127.0f);
-    if (on) st_v4(q + t * H + 16 * c, quant16(a0, a1, scale));
+    if (on) st_v4(q + t * H + 16 * c, quant16_coded(a0, a1, scale, __frcp_rn(scale)));
     if (c == 0) scales[t] = scale;
     buf ^= 1;
   }
+}
+
+int g_occ_combine[4][64];
+
+template <bool INT8, int LOADS>
+cudaError_t launch_combine_t(const CombineArgs& a, int sms, int* cache, cudaStream_t s) {
+  constexpr int kBlock = 256;
+  const int per_sm = resident_ctas(combine_kernel<INT8, LOADS>, kBlock, 0, cache);
+  const int64_t warps_needed = a.T;
+  const int64_t blocks_needed = (warps_needed + kBlock / 32 - 1) / (kBlock / 32);
+  const int64_t want = static_cast<int64_t>(sms) * per_sm;
+  const int grid = static_cast<int>(blocks_needed < want ? blocks_needed : want);
+  combine_kernel<INT8, LOADS><<<grid, kBlock, 0, s>>>(a);
+  return cudaGetLastError();
 }
 
 }  // namespace
 
 cudaError_t launch_combine(const CombineArgs& a, int sms, cudaStream_t s) {
   if (a.T == 0) return cudaSuccess;
-  const int nchunk = a.H / 8;
-  int block = ((nchunk + 31) / 32) * 32;
-  if (block > 1024) block = 1024;
-  const int per_sm = 2048 / block;
-  const int64_t want = static_cast<int64_t>(sms) * per_sm;
-  const int grid = static_cast<int>(a.T < want ? a.T : want);
+  // 16 loads in flight per lane once a row is long enough to keep them busy
+  const int nchunk = a.int8_out ? a.H / 16 : a.H / 8;
+  const bool deep = nchunk >= 64;
   if (a.int8_out)
-    combine_kernel<true><<<grid, block, 0, s>>>(a);
-  else
-    combine_kernel<false><<<grid, block, 0, s>>>(a);
-  return cudaGetLastError();
+    return deep ? launch_combine_t<true, 16>(a, sms, g_occ_combine[0], s)
+                : launch_combine_t<true, 8>(a, sms, g_occ_combine[1], s);
+  return deep ? launch_combine_t<false, 16>(a, sms, g_occ_combine[2], s)
+              : launch_combine_t<false, 8>(a, sms, g_occ_combine[3], s);
 }
 
 cudaError_t launch_quantize_rows(const void* in, int64_t n, int H, int8_t* q, float* scales, int sms,
                                  cudaStream_t s) {
   if (n == 0) return cudaSuccess;
   const int block = ((H / 16 + 31) / 32) * 32;
-  const int per_sm = 2048 / block;
+  static int occ[32][64];  // per block size / 32 and device
+  const int per_sm = resident_ctas(quantize_rows_kernel, block, 0, occ[block / 32 - 1]);
   const int64_t want = static_cast<int64_t>(sms) * per_sm;
   const int grid = static_cast<int>(n < want ? n : want);
   quantize_rows_kernel<<<grid, block, 0, s>>>(in, n, H, q, scales);

@@ -7,7 +7,7 @@
 // running sums of the counts (NCCL EP article, hotelren.com, §3.3), and the
 // payload may be the token's per-token int8 code (ThunderEP §2.3).
 //
-// Four launches, so that every destination row is decided before any
+// Three launches, so that every destination row is decided before any
 // payload byte moves and the scatter is a pure read-once / write-k stream:
 //   count    one CTA per tile of `tile` tokens: per-expert bit masks of the
 //            tile's tokens in shared memory (atomicOr, order-free); their
@@ -18,12 +18,14 @@
 //            the last CTA to finish (atomic ticket after a fence — no CTA
 //            ever waits for another) sums the kept counts over experts into
 //            expert_off / rank_off;
-//   rows     one thread per (token, slot): row = expert_off[e] + position,
-//            or -1 past the cap; writes slot_row and row_slot;
-//   scatter  a grid-stride loop over tokens, one CTA per token row in
-//            flight: 16 elements per thread, 16-byte loads of x and of the
-//            next token's slot_row prefetched during this token, amax by warp
-//            shuffles and one shared step, IEEE scale/code, k 16-byte stores.
+//   scatter  a grid-stride loop over tokens. Threads j < k turn the token's
+//            pairs into rows (row = expert_off[e] + tile base + rank in
+//            tile, or -1 past the cap) and write slot_row / row_slot, two
+//            tokens ahead. int8: one CTA per token, 32 elements per thread,
+//            the next token's row loaded while this one is coded (exact amax,
+//            IEEE scale, exact int8 code), one 16-byte store per kept row and
+//            group. bf16: one warp per token, each 16-byte chunk of x loaded
+//            once and stored to every kept row.
 #include "ep_internal.h"
 
 namespace ep {
@@ -157,99 +159,230 @@ __global__ void __launch_bounds__(256) scan_kernel(const int32_t* __restrict__ t
   }
 }
 
-__global__ void __launch_bounds__(256) rows_kernel(const int32_t* __restrict__ idx, const int32_t* __restrict__ lrank,
-                                                    const int32_t* __restrict__ tile_base,
-                                                    const int32_t* __restrict__ expert_off, int64_t npairs, int E,
-                                                    int k, int tile_log2, int ntiles, int cap,
-                                                    int32_t* __restrict__ slot_row, int32_t* __restrict__ row_slot) {
-  for (int64_t p = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; p < npairs;
-       p += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-    const int e = idx[p];
-    const int lr = lrank[p];
-    int row = -1;
-    if (static_cast<unsigned>(e) < static_cast<unsigned>(E) && lr >= 0) {
-      const int64_t t = p / k;
-      const int pos = tile_base[static_cast<int64_t>(e) * ntiles + (t >> tile_log2)] + lr;
-      if (pos < cap) row = expert_off[e] + pos;
-    }
-    slot_row[p] = row;
-    if (row >= 0) row_slot[row] = static_cast<int32_t>(p);
+// Destination row of pair p = t*k + j, formed in three steps that the
+// scatter spreads over three tokens so that no step waits on the load issued
+// by the step before it within one token's time:
+//   A  load the pair's expert e and rank within its tile (from count);
+//   B  load the tile's first position within e and e's offset (from scan);
+//   C  row = offset + position if position < cap, else -1 (dropped); write
+//      slot_row and row_slot.
+// A bad expert id (already reported by count) gives row -1.
+struct PairA {
+  int e, lr;
+};
+struct PairB {
+  int pos, off;  // pos < 0: no row
+};
+
+__device__ __forceinline__ PairA pair_load_a(const DispatchArgs& a, int64_t t, int j) {
+  PairA r{-1, -1};
+  if (t < a.T) {
+    const int64_t p = t * a.k + j;
+    r.e = a.topk_idx[p];
+    r.lr = a.lrank[p];
+  }
+  return r;
+}
+
+__device__ __forceinline__ PairB pair_load_b(const DispatchArgs& a, int64_t t, PairA x, int tile_log2) {
+  PairB r{-1, 0};
+  if (t < a.T && static_cast<unsigned>(x.e) < static_cast<unsigned>(a.E) && x.lr >= 0) {
+    r.pos = a.tile_base[static_cast<int64_t>(x.e) * a.ntiles + (t >> tile_log2)] + x.lr;
+    r.off = a.expert_off[x.e];
+  }
+  return r;
+}
+
+__device__ __forceinline__ int pair_finish(const DispatchArgs& a, int64_t t, int j, PairB x) {
+  if (t >= a.T) return -1;
+  const int64_t p = t * a.k + j;
+  const int row = (x.pos >= 0 && x.pos < a.cap) ? x.off + x.pos : -1;
+  a.slot_row[p] = row;
+  if (row >= 0) a.row_slot[row] = static_cast<int32_t>(p);
+  return row;
+}
+
+constexpr unsigned kFull = 0xffffffffu;
+
+// Gathers the next (up to) 8 kept slots of `mask` (lowest slot first) from
+// the lanes that hold them: their payload row addresses, in every lane.
+__device__ __forceinline__ int gather_rows(unsigned& mask, int row, char* base, int64_t row_bytes, char* (&p)[8]) {
+  int n = 0;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const int src = mask ? __ffs(mask) - 1 : 0;  // uniform across the warp
+    const int r = __shfl_sync(kFull, row, src);
+    p[i] = base + static_cast<int64_t>(r < 0 ? 0 : r) * row_bytes;
+    if (mask) ++n;
+    mask &= mask - 1u;
+  }
+  return n;
+}
+
+// 32 bytes (16 bf16) of x per thread: one 32-byte load when the row base is
+// 32-byte aligned (V8), else two 16-byte loads.
+template <bool V8>
+__device__ __forceinline__ void ld_x32(const char* p, uint4& lo, uint4& hi) {
+  if constexpr (V8) {
+    asm volatile("ld.global.nc.L1::no_allocate.v8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+                 : "=r"(lo.x), "=r"(lo.y), "=r"(lo.z), "=r"(lo.w), "=r"(hi.x), "=r"(hi.y), "=r"(hi.z), "=r"(hi.w)
+                 : "l"(p));
+  } else {
+    lo = ld_stream_v4(p);
+    hi = ld_stream_v4(p + 16);
   }
 }
 
-template <bool INT8>
-__global__ void __launch_bounds__(1024) scatter_kernel(const DispatchArgs a) {
+// int8 payload: one CTA per token in flight (grid-stride). Thread c codes the
+// 16-element groups c and c + blockDim.x of the row, so that every warp-wide
+// store covers whole 32-byte sectors. The next token's row is loaded while
+// this one is coded; threads j < k carry slot j's row (rows pipeline above,
+// two tokens ahead). amax: exact per-thread halfword maxima, a warp max and one
+// shared-memory step; scale = amax/127 with IEEE division; the code is the
+// branch-free corrected-quotient path (quant16_coded).
+template <bool V8>
+__global__ void __launch_bounds__(512) scatter_int8_kernel(const DispatchArgs a, int tile_log2) {
+  constexpr int G = 2;  // 16-element groups per thread
   __shared__ int32_t rows_s[2][32];
-  __shared__ float amax_s[2][32];
+  __shared__ float amax_s[2][16];
   const int c = threadIdx.x;
-  const int nchunk = a.H >> 4;  // 16 elements per thread
-  const bool on = c < nchunk;
-  const int warp = c >> 5, lane = c & 31, nw = blockDim.x >> 5;
+  const int B = blockDim.x;
+  const int ngroup = a.H >> 4;
+  const bool slot = c < a.k;
+  const int warp = c >> 5, lane = c & 31, nw = B >> 5;
   const char* xb = static_cast<const char*>(a.x);
-
-  int64_t t = blockIdx.x;
-  uint4 a0 = make_uint4(0, 0, 0, 0), a1 = a0;
-  int my_row = -1;  // threads c < k: destination row of slot c of token t
-  if (t < a.T) {
-    if (on) {
-      const char* p = xb + (t * a.H + 16 * c) * 2;
-      a0 = ld_stream_v4(p);
-      a1 = ld_stream_v4(p + 16);
+  const int64_t GS = gridDim.x;
+  auto ld_tok = [&](int64_t t, uint4 (&v)[2 * G]) {
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+      const int grp = c + g * B;
+      if (t < a.T && grp < ngroup)
+        ld_x32<V8>(xb + (t * a.H + 16 * grp) * 2, v[2 * g], v[2 * g + 1]);
+      else
+        v[2 * g] = v[2 * g + 1] = make_uint4(0, 0, 0, 0);
     }
-    if (c < a.k) my_row = a.slot_row[t * a.k + c];
+  };
+  int64_t t = blockIdx.x;
+  uint4 cur[2 * G];
+  ld_tok(t, cur);
+  int my_row = -1;
+  PairB b_next{-1, 0};
+  PairA a_next2{-1, -1};
+  if (slot) {
+    my_row = pair_finish(a, t, c, pair_load_b(a, t, pair_load_a(a, t, c), tile_log2));
+    b_next = pair_load_b(a, t + GS, pair_load_a(a, t + GS, c), tile_log2);
+    a_next2 = pair_load_a(a, t + 2 * GS, c);
   }
   int buf = 0;
-  for (; t < a.T; t += gridDim.x) {
-    // prefetch the next token's x chunk and slot rows while this one is coded
-    const int64_t tn = t + gridDim.x;
-    uint4 n0 = make_uint4(0, 0, 0, 0), n1 = n0;
+  for (; t < a.T; t += GS) {
+    const int64_t tn = t + GS;
+    uint4 nxt[2 * G];
+    ld_tok(tn, nxt);
     int next_row = -1;
-    if (tn < a.T) {
-      if (on) {
-        const char* p = xb + (tn * a.H + 16 * c) * 2;
-        n0 = ld_stream_v4(p);
-        n1 = ld_stream_v4(p + 16);
-      }
-      if (c < a.k) next_row = a.slot_row[tn * a.k + c];
+    if (slot) {
+      rows_s[buf][c] = my_row;
+      next_row = pair_finish(a, tn, c, b_next);
+      b_next = pair_load_b(a, tn + GS, a_next2, tile_log2);
+      a_next2 = pair_load_a(a, tn + 2 * GS, c);
     }
-    if (c < a.k) rows_s[buf][c] = my_row;
-    float scale = 0.f;
-    if constexpr (INT8) {
-      float m = on ? fmaxf(absmax_bf16x8(a0), absmax_bf16x8(a1)) : 0.f;
-      m = warp_max(m);
-      if (lane == 0) amax_s[buf][warp] = m;
-      __syncthreads();
-      float am = amax_s[buf][0];
-      for (int i = 1; i < nw; ++i) am = fmaxf(am, amax_s[buf][i]);
-      scale = __fdiv_rn(am, 127.0f);
-    } else {
-      __syncthreads();
-    }
-    if (on) {
-      if constexpr (INT8) {
-        const uint4 q = quant16(a0, a1, scale);
-        for (int j = 0; j < a.k; ++j) {
-          const int row = rows_s[buf][j];
-          if (row >= 0) st_v4(static_cast<int8_t*>(a.payload) + static_cast<int64_t>(row) * a.H + 16 * c, q);
-        }
-      } else {
-        for (int j = 0; j < a.k; ++j) {
-          const int row = rows_s[buf][j];
-          if (row >= 0) {
-            char* p = static_cast<char*>(a.payload) + (static_cast<int64_t>(row) * a.H + 16 * c) * 2;
-            st_v4(p, a0);
-            st_v4(p + 16, a1);
-          }
-        }
+    float m = 0.f;
+#pragma unroll
+    for (int g = 0; g < G; ++g) m = fmaxf(m, absmax_bf16x16(cur[2 * g], cur[2 * g + 1]));
+    m = warp_max(m);
+    if (lane == 0) amax_s[buf][warp] = m;
+    __syncthreads();
+    float am = amax_s[buf][0];
+    for (int i = 1; i < nw; ++i) am = fmaxf(am, amax_s[buf][i]);
+    const float scale = __fdiv_rn(am, 127.0f);
+    const float inv = __frcp_rn(scale);
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+      const int grp = c + g * B;
+      if (grp >= ngroup) break;
+      const uint4 q = quant16_coded(cur[2 * g], cur[2 * g + 1], scale, inv);
+      for (int j = 0; j < a.k; ++j) {
+        const int row = rows_s[buf][j];
+        if (row >= 0) st_v4(static_cast<int8_t*>(a.payload) + static_cast<int64_t>(row) * a.H + 16 * grp, q);
       }
     }
-    if constexpr (INT8) {
-      if (c < a.k && my_row >= 0) a.scales[my_row] = scale;
-    }
-    a0 = n0;
-    a1 = n1;
+    if (slot && my_row >= 0) a.scales[my_row] = scale;
+#pragma unroll
+    for (int i = 0; i < 2 * G; ++i) cur[i] = nxt[i];
     my_row = next_row;
     buf ^= 1;
+  }
+}
+
+// bf16 payload: one warp per token in flight; no block-level synchronisation.
+// Lanes j < k carry slot j's row (rows pipeline over this warp's tokens t,
+// t+W, t+2W); a ballot keeps the slots that were not dropped and their row
+// addresses are gathered into every lane, so a token with no kept slot costs
+// nothing; each 16-byte chunk of x is loaded once (8 chunks per lane in
+// flight) and stored to every kept row.
+__global__ void __launch_bounds__(256) scatter_bf16_kernel(const DispatchArgs a, int tile_log2) {
+  constexpr int U = 8;  // 16-byte chunks per lane per pass
+  const int lane = threadIdx.x & 31;
+  const int64_t W = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
+  const int64_t w0 = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  const bool slot = lane < a.k;
+  const int64_t row_bytes = 2 * static_cast<int64_t>(a.H);
+  const int nchunk = a.H >> 3;  // 16-byte chunks (8 elements)
+  char* const pbase = static_cast<char*>(a.payload);
+
+  int my_row = -1;
+  PairB b_next{-1, 0};
+  PairA a_next2{-1, -1};
+  if (slot) {
+    my_row = pair_finish(a, w0, lane, pair_load_b(a, w0, pair_load_a(a, w0, lane), tile_log2));
+    b_next = pair_load_b(a, w0 + W, pair_load_a(a, w0 + W, lane), tile_log2);
+    a_next2 = pair_load_a(a, w0 + 2 * W, lane);
+  }
+  for (int64_t t = w0; t < a.T; t += W) {
+    const int row = my_row;
+    if (slot) {
+      my_row = pair_finish(a, t + W, lane, b_next);
+      b_next = pair_load_b(a, t + 2 * W, a_next2, tile_log2);
+      a_next2 = pair_load_a(a, t + 3 * W, lane);
+    }
+    const unsigned kept = __ballot_sync(kFull, row >= 0);
+    if (kept == 0u) continue;  // every copy of this token was dropped
+    const int nk = __popc(kept);
+    const char* xr = static_cast<const char*>(a.x) + t * row_bytes;
+    char* p[8];
+    if (nk <= 8) {
+      unsigned msk = kept;
+      gather_rows(msk, row, pbase, row_bytes, p);
+      for (int c0 = lane; c0 < nchunk; c0 += 32 * U) {
+        uint4 v[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+          const int c = c0 + 32 * u;
+          v[u] = c < nchunk ? ld_stream_v4(xr + 16 * static_cast<int64_t>(c)) : make_uint4(0, 0, 0, 0);
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+          const int c = c0 + 32 * u;
+          if (c >= nchunk) break;
+#pragma unroll
+          for (int i = 0; i < 8; ++i)
+            if (i < nk) st_v4(p[i] + 16 * static_cast<int64_t>(c), v[u]);
+        }
+      }
+    } else {
+      // more than 8 kept slots (k > 8): groups of 8 per chunk; the loop bound
+      // is warp-uniform because the gathers shuffle across all lanes
+      for (int c0 = 0; c0 < nchunk; c0 += 32) {
+        const int c = c0 + lane;
+        const uint4 v = c < nchunk ? ld_stream_v4(xr + 16 * static_cast<int64_t>(c)) : make_uint4(0, 0, 0, 0);
+        unsigned msk = kept;
+        while (msk) {
+          const int n = gather_rows(msk, row, pbase, row_bytes, p);
+#pragma unroll
+          for (int i = 0; i < 8; ++i)
+            if (i < n && c < nchunk) st_v4(p[i] + 16 * static_cast<int64_t>(c), v);
+        }
+      }
+    }
   }
 }
 
@@ -282,24 +415,29 @@ cudaError_t launch_dispatch(const DispatchArgs& a, int sms, cudaStream_t s) {
   if ((err = cudaGetLastError()) != cudaSuccess) return err;
   if (a.T == 0) return cudaSuccess;
 
-  const int64_t npairs = static_cast<int64_t>(a.T) * a.k;
-  const int64_t rblocks_need = (npairs + 255) / 256;
-  const int64_t rblocks_cap = static_cast<int64_t>(sms) * 8;
   const int tile_log2 = __builtin_ctz(static_cast<unsigned>(a.tile));
-  rows_kernel<<<static_cast<int>(rblocks_need < rblocks_cap ? rblocks_need : rblocks_cap), 256, 0, s>>>(
-      a.topk_idx, a.lrank, a.tile_base, a.expert_off, npairs, a.E, a.k, tile_log2, a.ntiles, a.cap, a.slot_row,
-      a.row_slot);
-  if ((err = cudaGetLastError()) != cudaSuccess) return err;
-
-  const int nchunk = a.H / 16;
-  const int block = ((nchunk + 31) / 32) * 32;
-  const int per_sm = block >= 2048 ? 1 : 2048 / block;
-  const int64_t want = static_cast<int64_t>(sms) * per_sm;
-  const int grid = static_cast<int>(a.T < want ? a.T : want);
-  if (a.int8)
-    scatter_kernel<true><<<grid, block, 0, s>>>(a);
-  else
-    scatter_kernel<false><<<grid, block, 0, s>>>(a);
+  if (a.int8) {
+    // two 16-element groups per thread: H/32 threads per token, >= 32 >= k
+    const int block = ((a.H / 32 + 31) / 32) * 32;
+    const bool v8 = (reinterpret_cast<uintptr_t>(a.x) & 31u) == 0;  // rows are then 32-byte aligned too
+    static int occ[2][16][64];  // per load width, block size / 32, device
+    const int per_sm = v8 ? resident_ctas(scatter_int8_kernel<true>, block, 0, occ[1][block / 32 - 1])
+                          : resident_ctas(scatter_int8_kernel<false>, block, 0, occ[0][block / 32 - 1]);
+    const int64_t want = static_cast<int64_t>(sms) * per_sm;
+    const int grid = static_cast<int>(a.T < want ? a.T : want);
+    if (v8)
+      scatter_int8_kernel<true><<<grid, block, 0, s>>>(a, tile_log2);
+    else
+      scatter_int8_kernel<false><<<grid, block, 0, s>>>(a, tile_log2);
+  } else {
+    constexpr int kBlock = 256;
+    static int occ[64];
+    const int per_sm = resident_ctas(scatter_bf16_kernel, kBlock, 0, occ);
+    const int64_t want = static_cast<int64_t>(sms) * per_sm;
+    const int64_t need = (static_cast<int64_t>(a.T) + kBlock / 32 - 1) / (kBlock / 32);
+    const int grid = static_cast<int>(need < want ? need : want);
+    scatter_bf16_kernel<<<grid, kBlock, 0, s>>>(a, tile_log2);
+  }
   return cudaGetLastError();
 }
 

@@ -89,6 +89,84 @@ __device__ __forceinline__ uint4 quant16(uint4 a0, uint4 a1, float scale) {
   return r;
 }
 
+// The same code without a division per element, for a scale of at least
+// 2^-100. With inv = 1/scale rounded to nearest, the quotient estimate
+// q0 = fl(x * inv) is corrected once with its exact remainder,
+// rem = fma(-q0, scale, x), as q1 = fma(rem, inv, q0) (the classic
+// remainder-based correction of a division by multiplication with a rounded
+// reciprocal), and q = rint(q1) is formed by adding 1.5 * 2^23, which rounds
+// to nearest-even at unit spacing for |q1| < 2^22 and leaves q in the low
+// byte of the sum's bits. rint(q1) equals rint(fl(x / scale)) for every bf16
+// amax with amax/127 >= 2^-100 and every bf16 |x| <= amax: checked
+// exhaustively on the host (523,237,695 pairs, no mismatch) and on the GPU by
+// the tests. Without the correction, 5,304 of those pairs round differently.
+// |q| <= 127 on that domain, so the clamp never binds. Two elements are
+// processed per packed fp32x2 instruction (mul/fma/add .rn.f32x2: IEEE
+// round-to-nearest per element, denormals kept).
+constexpr float kFastScaleMin = 0x1p-100f;
+
+__device__ __forceinline__ uint64_t f32x2_pack(uint32_t lo, uint32_t hi) {
+  return (static_cast<uint64_t>(hi) << 32) | lo;
+}
+__device__ __forceinline__ uint64_t f32x2_mul(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ uint64_t f32x2_fma(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t r;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+  return r;
+}
+__device__ __forceinline__ uint64_t f32x2_add(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+
+__device__ __forceinline__ uint32_t pack4_low_bytes(uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+  return __byte_perm(__byte_perm(a, b, 0x0040), __byte_perm(c, d, 0x0040), 0x5410);
+}
+
+// 16 bf16 -> 16 int8 codes by the corrected-quotient path (scale >= 2^-100).
+__device__ __forceinline__ uint4 quant16_fast(uint4 a0, uint4 a1, float scale, float inv) {
+  const uint64_t inv2 = f32x2_pack(__float_as_uint(inv), __float_as_uint(inv));
+  const uint64_t nsc2 = f32x2_pack(__float_as_uint(-scale), __float_as_uint(-scale));
+  const uint64_t mg2 = f32x2_pack(0x4B400000u, 0x4B400000u);  // 1.5 * 2^23 in both halves
+  const uint32_t w[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+  uint32_t tb[16];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const uint64_t x2 = f32x2_pack(w[i] << 16, w[i] & 0xffff0000u);  // (lower, upper) element
+    const uint64_t q0 = f32x2_mul(x2, inv2);
+    const uint64_t rem = f32x2_fma(q0, nsc2, x2);
+    const uint64_t t = f32x2_add(f32x2_fma(rem, inv2, q0), mg2);
+    tb[2 * i] = static_cast<uint32_t>(t);
+    tb[2 * i + 1] = static_cast<uint32_t>(t >> 32);
+  }
+  return make_uint4(pack4_low_bytes(tb[0], tb[1], tb[2], tb[3]), pack4_low_bytes(tb[4], tb[5], tb[6], tb[7]),
+                    pack4_low_bytes(tb[8], tb[9], tb[10], tb[11]), pack4_low_bytes(tb[12], tb[13], tb[14], tb[15]));
+}
+
+// The int8 code of 16 elements given the row's scale and inv = 1/scale
+// (rounded to nearest): the corrected-quotient path, or IEEE division for
+// the tiny scales where it is not covered.
+__device__ __forceinline__ uint4 quant16_coded(uint4 a0, uint4 a1, float scale, float inv) {
+  if (scale >= kFastScaleMin) return quant16_fast(a0, a1, scale, inv);
+  return quant16(a0, a1, scale);
+}
+
+// max |x| over 16 bf16 (two 16-byte words). With the sign bits cleared, the
+// bit patterns of non-negative floats order like unsigned integers (subnormals
+// included), so a per-halfword unsigned max gives the exact maximum.
+__device__ __forceinline__ float absmax_bf16x16(uint4 a0, uint4 a1) {
+  const uint32_t m = 0x7fff7fffu;
+  uint32_t r = __vmaxu2(__vmaxu2(a0.x & m, a0.y & m), __vmaxu2(a0.z & m, a0.w & m));
+  r = __vmaxu2(r, __vmaxu2(__vmaxu2(a1.x & m, a1.y & m), __vmaxu2(a1.z & m, a1.w & m)));
+  const uint32_t hi = r >> 16, lo = r & 0xffffu;
+  return __uint_as_float((hi > lo ? hi : lo) << 16);
+}
+
 __device__ __forceinline__ float absmax_bf16x8(uint4 a) {
   float m = fabsf(bf16_lo(a.x));
   m = fmaxf(m, fabsf(bf16_hi(a.x)));

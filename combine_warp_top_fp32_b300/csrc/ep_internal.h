@@ -47,6 +47,22 @@ inline WsLayout ws_layout(int T, int E, int k) {
   return L;
 }
 
+// CTAs of `kernel` (at `block` threads, `smem` dynamic shared bytes) that fit
+// on one SM at once, cached per device in cache[64]; 1 if the query fails. A
+// grid-stride kernel launched with sms * this many CTAs runs in one wave: a
+// larger grid would leave a second, partial wave that starts only when whole
+// CTAs of the first one have finished all their work.
+template <typename K>
+inline int resident_ctas(K kernel, int block, int smem, int* cache) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return 1;
+  if (dev < 64 && cache[dev] > 0) return cache[dev];
+  int n = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, block, smem) != cudaSuccess || n < 1) n = 1;
+  if (dev < 64) cache[dev] = n;
+  return n;
+}
+
 cudaError_t launch_route(const float* logits, int T, int E, int k, int renorm, int32_t* idx, float* w, int sms,
                          cudaStream_t s);
 

@@ -217,7 +217,8 @@ cudaError_t launch_route_t(const float* logits, int T, int E, int k, int lanes_l
   const int groups_per_warp = 32 >> lanes_log2;
   const int64_t warps = (static_cast<int64_t>(T) + groups_per_warp - 1) / groups_per_warp;
   const int64_t blocks_needed = (warps + 7) / 8;
-  const int64_t cap_blocks = static_cast<int64_t>(sms) * 8;
+  static int occ[64];  // one cache per template instance
+  const int64_t cap_blocks = static_cast<int64_t>(sms) * resident_ctas(route_topk_kernel<VPL, VEC4>, 256, 0, occ);
   const int grid = static_cast<int>(blocks_needed < cap_blocks ? blocks_needed : cap_blocks);
   route_topk_kernel<VPL, VEC4><<<grid, 256, 0, s>>>(logits, T, E, k, lanes_log2, renorm, idx, w);
   return cudaGetLastError();
