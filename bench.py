@@ -267,7 +267,7 @@ def workload_config(w, payload, n_rows, eager=False):
             "payload": payload, "expert_out": "bf16", "rows_dispatched": n_rows,
             "l2": "no flush: each step moves > 1 GB, far beyond the 126 MB L2",
             "parallelism": "replicas (R virtual ranks per GPU)",
-            "launch": "eager" if eager else "cuda-graph replay per stage"}
+            "launch": "eager" if eager else "one cuda graph of all timed steps, events between stages"}
 
 
 # ----------------------------------------------------------------------------
@@ -299,15 +299,29 @@ def run_gpu(args):
     torch.cuda.synchronize()
     assert ep.ep_get_error(buf.ws) == ep.EP_OK
     N = int(buf.rank_off[-1].item())
-    launches_per_step = 6 if w.T > 0 else 2  # route; count, scan, rows, scatter; combine
+    launches_per_step = 5 if w.T > 0 else 2  # route; count, scan, scatter; combine (count + scan when T = 0)
 
-    # The step's launches are captured once per stage as CUDA graphs (the
-    # library never synchronises or allocates, so its calls capture as they
-    # are); replaying them takes the host's per-call overhead off the GPU's
-    # critical path. Events between the three replays time each stage live.
+    # The timed region is one CUDA graph holding all K steps (the library's
+    # calls neither synchronise nor allocate, so they capture as they are):
+    # replaying it takes the host's per-call overhead off the GPU's critical
+    # path (the Sparse-communication article's §4.2 suggestion). Event-record
+    # nodes between the three calls of every step time each stage live.
     stage_fns = {"route": lambda: buf.route(logits), "dispatch": lambda: buf.dispatch(x),
                  "combine": lambda: buf.combine(eo)}
-    graphs = {}
+    ev = [[torch.cuda.Event(enable_timing=True, external=not args.eager) for _ in range(4)]
+          for _ in range(args.steps)]
+
+    def steps_with_events():
+        for i in range(args.steps):
+            ev[i][0].record()
+            stage_fns["route"]()
+            ev[i][1].record()
+            stage_fns["dispatch"]()
+            ev[i][2].record()
+            stage_fns["combine"]()
+            ev[i][3].record()
+
+    graph = None
     if not args.eager:
         side = torch.cuda.Stream()
         side.wait_stream(stream)
@@ -315,37 +329,29 @@ def run_gpu(args):
             for fn in stage_fns.values():
                 fn()
         stream.wait_stream(side)
-        for name, fn in stage_fns.items():
-            g = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(g):
-                fn()
-            graphs[name] = g
-        for _ in range(args.warmup):
-            for g in graphs.values():
-                g.replay()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            steps_with_events()
+        graph.replay()  # untimed warm-up pass of the captured steps
         torch.cuda.synchronize()
         assert ep.ep_get_error(buf.ws) == ep.EP_OK
-    run = {n: (graphs[n].replay if graphs else stage_fns[n]) for n in stage_fns}
 
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     sampler = ClockSampler(local)
     sampler.start()
     barrier()
     torch.cuda.synchronize()
-    for i in range(args.steps):
-        e = ev[i]
-        e[0].record(stream)
-        run["route"]()
-        e[1].record(stream)
-        run["dispatch"]()
-        e[2].record(stream)
-        run["combine"]()
-        e[3].record(stream)
+    t0.record(stream)
+    if graph is not None:
+        graph.replay()
+    else:
+        steps_with_events()
+    t1.record(stream)
     torch.cuda.synchronize()
     barrier()
     assert ep.ep_get_error(buf.ws) == ep.EP_OK
     clocks = sampler.stop()
-    total_ms = ev[0][0].elapsed_time(ev[-1][3])
+    total_ms = t0.elapsed_time(t1)
     stage_ms = {
         "route": sum(e[0].elapsed_time(e[1]) for e in ev) / args.steps,
         "dispatch": sum(e[1].elapsed_time(e[2]) for e in ev) / args.steps,
@@ -361,7 +367,7 @@ def run_gpu(args):
     step_gbs = nb["total"] / (ms_per_step / 1e3) / 1e9
     stage_gbs = {s: nb[s] / (stage_ms[s] / 1e3) / 1e9 for s in stage_ms}
     dominant = max(stage_ms, key=stage_ms.get)
-    kernel_names = {"route": "route_topk_kernel", "dispatch": "count+scan+rows+scatter_kernel",
+    kernel_names = {"route": "route_topk_kernel", "dispatch": "count+scan+scatter_kernel",
                     "combine": "combine_kernel<bf16>"}
     traffic = recorded_traffic(dominant, w.name, args.payload)
 
@@ -440,7 +446,7 @@ def parse_args(argv=None):
     ap.add_argument("--workload", default="capacity")
     ap.add_argument("--payload", choices=["int8", "bf16"], default=None)
     ap.add_argument("--no-e2e", action="store_true")
-    ap.add_argument("--eager", action="store_true", help="launch through the binding each step (no CUDA graphs)")
+    ap.add_argument("--eager", action="store_true", help="launch through the binding each step (no CUDA graph)")
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-baseline-s", type=float, default=15.0)

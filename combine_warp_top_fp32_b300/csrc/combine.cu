@@ -130,6 +130,8 @@ __global__ void __launch_bounds__(256) combine_kernel(const CombineArgs a) {
   const int nchunk = a.H / EL;
   const int64_t row_bytes = INT8 ? a.H : 2 * static_cast<int64_t>(a.H);
   const char* base = static_cast<const char*>(a.expert_out);
+  pdl_wait();  // slot rows, weights and expert outputs come from earlier kernels
+  pdl_launch_dependents();
 
   // lane j < k: slot j of token t (row, weight, scale); -1 / 0 elsewhere
   auto load_slot = [&](int64_t t, int& row, float& w, float& sc) {
@@ -203,6 +205,8 @@ __global__ void __launch_bounds__(1024) quantize_rows_kernel(const void* __restr
   const int c = threadIdx.x;
   const bool on = c < (H >> 4);
   const int warp = c >> 5, lane = c & 31, nw = blockDim.x >> 5;
+  pdl_wait();
+  pdl_launch_dependents();
   int buf = 0;
   for (int64_t t = blockIdx.x; t < n; t += gridDim.x) {
     uint4 a0 = make_uint4(0, 0, 0, 0), a1 = a0;
@@ -234,8 +238,7 @@ cudaError_t launch_combine_t(const CombineArgs& a, int sms, int* cache, cudaStre
   const int64_t blocks_needed = (warps_needed + kBlock / 32 - 1) / (kBlock / 32);
   const int64_t want = static_cast<int64_t>(sms) * per_sm;
   const int grid = static_cast<int>(blocks_needed < want ? blocks_needed : want);
-  combine_kernel<INT8, LOADS><<<grid, kBlock, 0, s>>>(a);
-  return cudaGetLastError();
+  return launch_pdl(combine_kernel<INT8, LOADS>, grid, kBlock, 0, s, a);
 }
 
 }  // namespace
@@ -260,8 +263,7 @@ cudaError_t launch_quantize_rows(const void* in, int64_t n, int H, int8_t* q, fl
   const int per_sm = resident_ctas(quantize_rows_kernel, block, 0, occ[block / 32 - 1]);
   const int64_t want = static_cast<int64_t>(sms) * per_sm;
   const int grid = static_cast<int>(n < want ? n : want);
-  quantize_rows_kernel<<<grid, block, 0, s>>>(in, n, H, q, scales);
-  return cudaGetLastError();
+  return launch_pdl(quantize_rows_kernel, grid, block, 0, s, in, n, H, q, scales);
 }
 
 }  // namespace ep

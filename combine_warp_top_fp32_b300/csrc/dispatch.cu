@@ -36,6 +36,8 @@ __global__ void __launch_bounds__(512) count_kernel(const int32_t* __restrict__ 
                                                     int32_t* __restrict__ lrank, uint32_t* status,
                                                     uint32_t* ticket) {
   extern __shared__ uint32_t smem[];
+  pdl_wait();  // the expert ids come from the kernel before this one
+  pdl_launch_dependents();
   if (blockIdx.x == 0 && threadIdx.x == 0) *ticket = 0u;  // the scan that follows counts its CTAs from 0
   const int TW = tile >> 5;
   uint32_t* mask = smem;         // [E][TW] bit b of word w: token 32*w+b of the tile chose e
@@ -112,6 +114,8 @@ __global__ void __launch_bounds__(256) scan_kernel(const int32_t* __restrict__ t
   __shared__ int warp_s[8];
   __shared__ int is_last;
   const int e = blockIdx.x;
+  pdl_wait();  // tile counts come from the count kernel
+  pdl_launch_dependents();
   // this expert's running sum over tiles
   int carry = 0;
   for (int c0 = 0; c0 < ntiles; c0 += blockDim.x) {
@@ -263,15 +267,23 @@ __global__ void __launch_bounds__(512) scatter_int8_kernel(const DispatchArgs a,
     }
   };
   int64_t t = blockIdx.x;
+  // Before the wait: x and the pair data of the count kernel (two launches
+  // back) only; tile bases and offsets come from the scan just before.
   uint4 cur[2 * G];
   ld_tok(t, cur);
+  PairA a0{-1, -1}, a1{-1, -1}, a_next2{-1, -1};
+  if (slot) {
+    a0 = pair_load_a(a, t, c);
+    a1 = pair_load_a(a, t + GS, c);
+    a_next2 = pair_load_a(a, t + 2 * GS, c);
+  }
+  pdl_wait();
+  pdl_launch_dependents();
   int my_row = -1;
   PairB b_next{-1, 0};
-  PairA a_next2{-1, -1};
   if (slot) {
-    my_row = pair_finish(a, t, c, pair_load_b(a, t, pair_load_a(a, t, c), tile_log2));
-    b_next = pair_load_b(a, t + GS, pair_load_a(a, t + GS, c), tile_log2);
-    a_next2 = pair_load_a(a, t + 2 * GS, c);
+    my_row = pair_finish(a, t, c, pair_load_b(a, t, a0, tile_log2));
+    b_next = pair_load_b(a, t + GS, a1, tile_log2);
   }
   int buf = 0;
   for (; t < a.T; t += GS) {
@@ -329,13 +341,19 @@ __global__ void __launch_bounds__(256) scatter_bf16_kernel(const DispatchArgs a,
   const int nchunk = a.H >> 3;  // 16-byte chunks (8 elements)
   char* const pbase = static_cast<char*>(a.payload);
 
+  PairA a0{-1, -1}, a1{-1, -1}, a_next2{-1, -1};
+  if (slot) {  // before the wait: pair data of the count kernel, two launches back
+    a0 = pair_load_a(a, w0, lane);
+    a1 = pair_load_a(a, w0 + W, lane);
+    a_next2 = pair_load_a(a, w0 + 2 * W, lane);
+  }
+  pdl_wait();  // tile bases and offsets come from the scan just before
+  pdl_launch_dependents();
   int my_row = -1;
   PairB b_next{-1, 0};
-  PairA a_next2{-1, -1};
   if (slot) {
-    my_row = pair_finish(a, w0, lane, pair_load_b(a, w0, pair_load_a(a, w0, lane), tile_log2));
-    b_next = pair_load_b(a, w0 + W, pair_load_a(a, w0 + W, lane), tile_log2);
-    a_next2 = pair_load_a(a, w0 + 2 * W, lane);
+    my_row = pair_finish(a, w0, lane, pair_load_b(a, w0, a0, tile_log2));
+    b_next = pair_load_b(a, w0 + W, a1, tile_log2);
   }
   for (int64_t t = w0; t < a.T; t += W) {
     const int row = my_row;
@@ -407,12 +425,12 @@ cudaError_t launch_dispatch(const DispatchArgs& a, int sms, cudaStream_t s) {
   }
   int cblock = ((a.tile * a.k + 31) / 32) * 32;
   cblock = cblock < 64 ? 64 : (cblock > 512 ? 512 : cblock);
-  count_kernel<<<a.ntiles > 0 ? a.ntiles : 1, cblock, smem, s>>>(a.topk_idx, a.T, a.E, a.k, a.tile, a.ntiles,
-                                                                 a.tile_counts, a.lrank, a.status, a.ticket);
-  if ((err = cudaGetLastError()) != cudaSuccess) return err;
-  scan_kernel<<<a.E, 256, 0, s>>>(a.tile_counts, a.E, a.R, a.ntiles, a.cap, a.tile_base, a.expert_counts,
-                                  a.expert_raw, a.expert_off, a.rank_off, a.n_dropped, a.kept, a.dropped, a.ticket);
-  if ((err = cudaGetLastError()) != cudaSuccess) return err;
+  err = launch_pdl(count_kernel, a.ntiles > 0 ? a.ntiles : 1, cblock, static_cast<size_t>(smem), s, a.topk_idx, a.T,
+                   a.E, a.k, a.tile, a.ntiles, a.tile_counts, a.lrank, a.status, a.ticket);
+  if (err != cudaSuccess) return err;
+  err = launch_pdl(scan_kernel, a.E, 256, 0, s, a.tile_counts, a.E, a.R, a.ntiles, a.cap, a.tile_base, a.expert_counts,
+                   a.expert_raw, a.expert_off, a.rank_off, a.n_dropped, a.kept, a.dropped, a.ticket);
+  if (err != cudaSuccess) return err;
   if (a.T == 0) return cudaSuccess;
 
   const int tile_log2 = __builtin_ctz(static_cast<unsigned>(a.tile));
@@ -425,10 +443,8 @@ cudaError_t launch_dispatch(const DispatchArgs& a, int sms, cudaStream_t s) {
                           : resident_ctas(scatter_int8_kernel<false>, block, 0, occ[0][block / 32 - 1]);
     const int64_t want = static_cast<int64_t>(sms) * per_sm;
     const int grid = static_cast<int>(a.T < want ? a.T : want);
-    if (v8)
-      scatter_int8_kernel<true><<<grid, block, 0, s>>>(a, tile_log2);
-    else
-      scatter_int8_kernel<false><<<grid, block, 0, s>>>(a, tile_log2);
+    err = v8 ? launch_pdl(scatter_int8_kernel<true>, grid, block, 0, s, a, tile_log2)
+             : launch_pdl(scatter_int8_kernel<false>, grid, block, 0, s, a, tile_log2);
   } else {
     constexpr int kBlock = 256;
     static int occ[64];
@@ -436,9 +452,9 @@ cudaError_t launch_dispatch(const DispatchArgs& a, int sms, cudaStream_t s) {
     const int64_t want = static_cast<int64_t>(sms) * per_sm;
     const int64_t need = (static_cast<int64_t>(a.T) + kBlock / 32 - 1) / (kBlock / 32);
     const int grid = static_cast<int>(need < want ? need : want);
-    scatter_bf16_kernel<<<grid, kBlock, 0, s>>>(a, tile_log2);
+    err = launch_pdl(scatter_bf16_kernel, grid, kBlock, 0, s, a, tile_log2);
   }
-  return cudaGetLastError();
+  return err;
 }
 
 }  // namespace ep

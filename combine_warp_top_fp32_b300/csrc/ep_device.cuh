@@ -15,6 +15,20 @@ __device__ __forceinline__ void raise_status(uint32_t* status, uint32_t bit) {
   atomicOr(status, bit);
 }
 
+// ---- programmatic dependent launch ----------------------------------------
+// Every kernel of the library is launched with programmatic stream
+// serialisation, so it may start while the kernel before it in the stream is
+// still finishing. pdl_wait() blocks until that kernel has completed and its
+// memory is visible (a no-op when there is no programmatic predecessor);
+// nothing the predecessor writes may be read, and nothing it reads or writes
+// may be written, before it. pdl_launch_dependents() lets the next kernel
+// start launching; each kernel calls it only after its own pdl_wait(), so by
+// induction everything older than the immediate predecessor has completed
+// once a kernel starts: its pre-wait code may read the outputs of kernels two
+// or more launches back.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // ---- 16-byte global memory access ----------------------------------------
 // Streaming read of data that this kernel touches once: skip L1 allocation.
 __device__ __forceinline__ uint4 ld_stream_v4(const void* p) {

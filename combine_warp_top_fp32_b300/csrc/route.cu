@@ -14,7 +14,9 @@
 //   - k rounds of: lane-local max, group max, the owner clears the winning
 //     key; lane j keeps slot j. With one token per warp (E >= 32) the group
 //     max is two redux.sync reductions (value max, then lowest id holding
-//     it); with several tokens per warp it is a __shfl_xor_sync butterfly;
+//     it), and for E <= 256 each lane sorts its keys once so that its local
+//     max is always its first key; with several tokens per warp the group max
+//     is a __shfl_xor_sync butterfly;
 //   - softmax denominator: exp(l - l_max) with the subtraction's rounding
 //     error carried into the exponential, summed with compensated (Neumaier /
 //     TwoSum) arithmetic, so the weight stays within 1e-6 of the exact value.
@@ -46,6 +48,32 @@ __device__ __forceinline__ int key_expert(uint64_t key) {
 }
 
 __device__ __forceinline__ uint64_t umax64(uint64_t a, uint64_t b) { return a > b ? a : b; }
+
+// Compare-exchange so that key[i] >= key[j].
+template <int N>
+__device__ __forceinline__ void cx(uint64_t (&key)[N], int i, int j) {
+  const uint64_t a = key[i], b = key[j];
+  key[i] = a > b ? a : b;
+  key[j] = a > b ? b : a;
+}
+
+// Sorts a lane's keys in descending order (fixed networks: Batcher's
+// odd-even merge sort for 8, its 5-exchange form for 4).
+template <int N>
+__device__ __forceinline__ void sort_desc(uint64_t (&key)[N]) {
+  if constexpr (N == 2) {
+    cx(key, 0, 1);
+  } else if constexpr (N == 4) {
+    cx(key, 0, 1); cx(key, 2, 3); cx(key, 0, 2); cx(key, 1, 3); cx(key, 1, 2);
+  } else if constexpr (N == 8) {
+    cx(key, 0, 1); cx(key, 2, 3); cx(key, 4, 5); cx(key, 6, 7);
+    cx(key, 0, 2); cx(key, 1, 3); cx(key, 4, 6); cx(key, 5, 7);
+    cx(key, 1, 2); cx(key, 5, 6);
+    cx(key, 0, 4); cx(key, 1, 5); cx(key, 2, 6); cx(key, 3, 7);
+    cx(key, 2, 4); cx(key, 3, 5);
+    cx(key, 1, 2); cx(key, 3, 4); cx(key, 5, 6);
+  }
+}
 
 // exp(v - m) with the rounding error of the subtraction folded back in:
 // v - m = d + err exactly (TwoSum), exp(d + err) ~= exp(d) * (1 + err).
@@ -94,6 +122,8 @@ __global__ void __launch_bounds__(256) route_topk_kernel(const float* __restrict
   const int grp = lane >> lanes_log2;
   const int64_t warp_id = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
   const int64_t n_warps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
+  pdl_wait();  // the logits may come from the kernel before this one
+  pdl_launch_dependents();
 
   for (int64_t tb = warp_id * groups_per_warp; tb < T; tb += n_warps * groups_per_warp) {
     const int64_t t = tb + grp;
@@ -131,7 +161,31 @@ __global__ void __launch_bounds__(256) route_topk_kernel(const float* __restrict
     int my_e = 0;
     float my_v = 0.f;
     float l_max = 0.f;
-    if (L == 32) {
+    if (L == 32 && VPL <= 8) {
+      // One token per warp, each lane's keys sorted once (largest first):
+      // every round the lanes offer their head key; redux.sync max over the
+      // value bits finds the largest logit, redux.sync min over the ids of
+      // the lanes offering it breaks the tie toward the lower expert id, and
+      // the winning lane drops its head (a shift of its sorted list).
+      sort_desc<VPL>(key);
+      for (int r = 0; r < k; ++r) {
+        const uint32_t hv = static_cast<uint32_t>(key[0] >> 32);
+        const uint32_t gmax = __reduce_max_sync(0xffffffffu, hv);
+        const uint32_t cand = (hv == gmax) ? 0xffffffffu - static_cast<uint32_t>(key[0]) : 0xffffffffu;
+        const uint32_t win = __reduce_min_sync(0xffffffffu, cand);
+        const float v = key_value(static_cast<uint64_t>(gmax) << 32);
+        if (r == 0) l_max = v;
+        if (sub == r) {
+          my_e = static_cast<int>(win);
+          my_v = v;
+        }
+        if (cand == win) {
+#pragma unroll
+          for (int i = 0; i + 1 < VPL; ++i) key[i] = key[i + 1];
+          key[VPL - 1] = 0ull;  // 0 is below every real key
+        }
+      }
+    } else if (L == 32) {
       // One token per warp: two single-instruction warp reductions per round.
       // redux.sync max over the order-preserving value bits finds the largest
       // logit, redux.sync min over the ids of the lanes holding it breaks the
@@ -220,8 +274,7 @@ cudaError_t launch_route_t(const float* logits, int T, int E, int k, int lanes_l
   static int occ[64];  // one cache per template instance
   const int64_t cap_blocks = static_cast<int64_t>(sms) * resident_ctas(route_topk_kernel<VPL, VEC4>, 256, 0, occ);
   const int grid = static_cast<int>(blocks_needed < cap_blocks ? blocks_needed : cap_blocks);
-  route_topk_kernel<VPL, VEC4><<<grid, 256, 0, s>>>(logits, T, E, k, lanes_log2, renorm, idx, w);
-  return cudaGetLastError();
+  return launch_pdl(route_topk_kernel<VPL, VEC4>, grid, 256, 0, s, logits, T, E, k, lanes_log2, renorm, idx, w);
 }
 
 }  // namespace
