@@ -242,7 +242,7 @@ def run_reference(args):
         "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "fp32",
-        "data": "synthetic", "config": workload_config(w, args.payload, None),
+        "data": "synthetic", "config": workload_config(w, args.payload, None, False, args.path),
         "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle", "sample": sample,
                          "cpu": cpu_model()},
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -261,13 +261,17 @@ def cpu_model():
     return f"unknown (nproc={os.cpu_count()})"
 
 
-def workload_config(w, payload, n_rows, eager=False):
+def workload_config(w, payload, n_rows, eager=False, path="fused"):
+    rows = n_rows if n_rows is not None else w.max_rows()
+    step_bytes = algorithmic_bytes(w.T, w.H, w.E, w.k, rows, payload == "int8")["total"]
+    l2 = (f"no flush: each step moves {step_bytes / 1e9:.2f} GB, beyond the 126 MB L2" if step_bytes > L2_BYTES else
+          f"not flushed: the {step_bytes / 1e6:.1f} MB step fits in the 126 MB L2 (latency-bound shape)")
     return {"workload": w.name, "T": w.T, "H": w.H, "E": w.E, "k": w.k, "R": w.R,
             "capacity_factor": w.capacity_factor, "cap": w.capacity() if w.capacity_factor > 0 else None,
-            "payload": payload, "expert_out": "bf16", "rows_dispatched": n_rows,
-            "l2": "no flush: each step moves > 1 GB, far beyond the 126 MB L2",
+            "payload": payload, "expert_out": "bf16", "rows_dispatched": n_rows, "l2": l2,
             "parallelism": "replicas (R virtual ranks per GPU)",
-            "launch": "eager" if eager else "one cuda graph of all timed steps, events between stages"}
+            "path": ("ep_route_dispatch + ep_combine" if path == "fused" else "ep_route + ep_dispatch + ep_combine"),
+            "launch": "eager" if eager else "one cuda graph of all timed steps; stage events on a side branch"}
 
 
 # ----------------------------------------------------------------------------
@@ -295,40 +299,63 @@ def run_gpu(args):
     stream = torch.cuda.current_stream()
 
     for _ in range(args.warmup):
-        buf.step(logits, x, eo)
+        if args.path == "fused":
+            buf.route_dispatch(logits, x)
+            buf.combine(eo)
+        else:
+            buf.step(logits, x, eo)
     torch.cuda.synchronize()
     assert ep.ep_get_error(buf.ws) == ep.EP_OK
     N = int(buf.rank_off[-1].item())
-    launches_per_step = 5 if w.T > 0 else 2  # route; count, scan, scatter; combine (count + scan when T = 0)
+    if args.path == "fused":
+        # ep_route_dispatch (route+count, scan, scatter) then ep_combine
+        launches_per_step = 4 if w.T > 0 else 2
+    else:
+        # ep_route; ep_dispatch (count, scan, scatter); ep_combine
+        launches_per_step = 5 if w.T > 0 else 2
 
     # The timed region is one CUDA graph holding all K steps (the library's
     # calls neither synchronise nor allocate, so they capture as they are):
     # replaying it takes the host's per-call overhead off the GPU's critical
-    # path (the Sparse-communication article's §4.2 suggestion). Event-record
-    # nodes between the three calls of every step time each stage live.
-    stage_fns = {"route": lambda: buf.route(logits), "dispatch": lambda: buf.dispatch(x),
-                 "combine": lambda: buf.combine(eo)}
-    ev = [[torch.cuda.Event(enable_timing=True, external=not args.eager) for _ in range(4)]
-          for _ in range(args.steps)]
+    # path (the Sparse-communication article's §4.2 suggestion), and the
+    # library's programmatic dependent launches overlap each kernel's launch
+    # with its predecessor's tail. Stage times are taken live by event-record
+    # nodes on a side branch of the graph: after each call the side stream
+    # waits on the main stream and records an event, and nothing waits on
+    # those events, so they do not break the chain of dependent launches.
+    # Stage i ends at its event; it starts where the previous stage ended.
+    if args.path == "fused":
+        stage_fns = {"route+dispatch": lambda: buf.route_dispatch(logits, x), "combine": lambda: buf.combine(eo)}
+    else:
+        stage_fns = {"route": lambda: buf.route(logits), "dispatch": lambda: buf.dispatch(x),
+                     "combine": lambda: buf.combine(eo)}
+    names = list(stage_fns)
+    ev_start = torch.cuda.Event(enable_timing=True, external=not args.eager)
+    ev = [[torch.cuda.Event(enable_timing=True, external=not args.eager) for _ in names] for _ in range(args.steps)]
+    side = torch.cuda.Stream()
 
     def steps_with_events():
+        main = torch.cuda.current_stream()
+        ev_start.record(main)
         for i in range(args.steps):
-            ev[i][0].record()
-            stage_fns["route"]()
-            ev[i][1].record()
-            stage_fns["dispatch"]()
-            ev[i][2].record()
-            stage_fns["combine"]()
-            ev[i][3].record()
+            for j, n in enumerate(names):
+                stage_fns[n]()
+                if args.eager:
+                    ev[i][j].record(main)
+                else:
+                    side.wait_stream(main)
+                    ev[i][j].record(side)
+        if not args.eager:
+            main.wait_stream(side)
 
     graph = None
     if not args.eager:
-        side = torch.cuda.Stream()
-        side.wait_stream(stream)
-        with torch.cuda.stream(side):
+        warm = torch.cuda.Stream()
+        warm.wait_stream(stream)
+        with torch.cuda.stream(warm):
             for fn in stage_fns.values():
                 fn()
-        stream.wait_stream(side)
+        stream.wait_stream(warm)
         graph = torch.cuda.CUDAGraph()
         with torch.cuda.graph(graph):
             steps_with_events()
@@ -352,22 +379,24 @@ def run_gpu(args):
     assert ep.ep_get_error(buf.ws) == ep.EP_OK
     clocks = sampler.stop()
     total_ms = t0.elapsed_time(t1)
-    stage_ms = {
-        "route": sum(e[0].elapsed_time(e[1]) for e in ev) / args.steps,
-        "dispatch": sum(e[1].elapsed_time(e[2]) for e in ev) / args.steps,
-        "combine": sum(e[2].elapsed_time(e[3]) for e in ev) / args.steps,
-    }
+    ends = [e for step in ev for e in step]
+    starts = [ev_start] + ends[:-1]
+    stage_ms = {n: 0.0 for n in names}
+    for q, (s0, s1) in enumerate(zip(starts, ends)):
+        stage_ms[names[q % len(names)]] += s0.elapsed_time(s1) / args.steps
     total_s = max_over_ranks(total_ms / 1e3)
     ms_per_step = 1e3 * total_s / args.steps
     tokens = w.T * args.steps * world
     value = tokens / total_s
 
     nb = algorithmic_bytes(w.T, w.H, w.E, w.k, N, p8)
+    nb["route+dispatch"] = nb["route"] + nb["dispatch"]
     peak, peak_src = measured_peak_gbs()
     step_gbs = nb["total"] / (ms_per_step / 1e3) / 1e9
     stage_gbs = {s: nb[s] / (stage_ms[s] / 1e3) / 1e9 for s in stage_ms}
     dominant = max(stage_ms, key=stage_ms.get)
     kernel_names = {"route": "route_topk_kernel", "dispatch": "count+scan+scatter_kernel",
+                    "route+dispatch": "route_count+scan+scatter_kernel",
                     "combine": "combine_kernel<bf16>"}
     traffic = recorded_traffic(dominant, w.name, args.payload)
 
@@ -385,7 +414,11 @@ def run_gpu(args):
             d_logits.copy_(h_logits, non_blocking=True)
             d_x.copy_(h_x, non_blocking=True)
             d_eo.copy_(h_eo, non_blocking=True)
-            buf.step(d_logits, d_x, d_eo)
+            if args.path == "fused":
+                buf.route_dispatch(d_logits, d_x)
+                buf.combine(d_eo)
+            else:
+                buf.step(d_logits, d_x, d_eo)
             h_y.copy_(buf.y, non_blocking=True)
 
         for _ in range(max(1, min(args.warmup, 3))):
@@ -419,7 +452,7 @@ def run_gpu(args):
         line = {
             "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "fp32", "data": "synthetic", "config": workload_config(w, args.payload, N, args.eager),
+            "vs_baseline": None, "dtype": "fp32", "data": "synthetic", "config": workload_config(w, args.payload, N, args.eager, args.path),
             "hbm": {"bytes_per_step": nb["total"], "gbs": step_gbs, "frac_of_8000": step_gbs / NOMINAL_HBM_GBS,
                     f"frac_of_{peak_src}": step_gbs / peak, "metadata_bytes_per_step": nb["metadata"]},
             "stages": {s: {"ms": stage_ms[s], "bytes": nb[s], "gbs": stage_gbs[s]} for s in stage_ms},
@@ -445,6 +478,8 @@ def parse_args(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="capacity")
     ap.add_argument("--payload", choices=["int8", "bf16"], default=None)
+    ap.add_argument("--path", choices=["calls", "fused"], default="fused",
+                    help="fused: ep_route_dispatch + ep_combine; calls: ep_route, ep_dispatch, ep_combine")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--eager", action="store_true", help="launch through the binding each step (no CUDA graph)")
     ap.add_argument("--e2e-steps", type=int, default=10)

@@ -31,7 +31,7 @@ EP_PAYLOAD_INT8 = 1
 EXPORTS = (
     "ep_status_string", "ep_config_check", "ep_capacity", "ep_max_rows", "ep_workspace_size",
     "ep_workspace_init", "ep_route", "ep_dispatch", "ep_combine", "ep_quantize_rows", "ep_get_error",
-    "ep_load_stats", "ep_dispatch_static",
+    "ep_load_stats", "ep_dispatch_static", "ep_route_dispatch",
 )
 
 
@@ -78,6 +78,7 @@ def _load():
     lib.ep_get_error.argtypes = [P, SZ, P]
     lib.ep_load_stats.argtypes = [P, I32, ctypes.POINTER(ep_load_stats_t)]
     lib.ep_dispatch_static.argtypes = [CFG, P, P, P, P, P, P, P, P, P, P, P, P]
+    lib.ep_route_dispatch.argtypes = [CFG, P, P, P, P, P, P, P, P, P, P, P, P, P, P, SZ, P]
     for name in EXPORTS:
         if name not in ("ep_status_string", "ep_max_rows"):
             getattr(lib, name).restype = ctypes.c_int
@@ -181,6 +182,21 @@ def ep_dispatch(cfg, x, topk_idx, payload, scales, row_slot, slot_row, expert_co
                            _ptr(ws, what="ws"), ws.numel() * ws.element_size(), _stream(stream)), "ep_dispatch")
 
 
+def ep_route_dispatch(cfg, logits, x, topk_idx, topk_w, payload, scales, row_slot, slot_row, expert_counts,
+                      expert_raw, expert_off, rank_off, n_dropped, ws, stream=None):
+    _check(lib.ep_route_dispatch(ctypes.byref(cfg), _ptr(logits, torch.float32, "logits"),
+                                 _ptr(x, torch.bfloat16, "x"), _ptr(topk_idx, torch.int32, "topk_idx"),
+                                 _ptr(topk_w, torch.float32, "topk_w"),
+                                 _ptr(payload, (torch.bfloat16, torch.int8), "payload"),
+                                 _ptr(scales, torch.float32, "scales"), _ptr(row_slot, torch.int32, "row_slot"),
+                                 _ptr(slot_row, torch.int32, "slot_row"),
+                                 _ptr(expert_counts, torch.int32, "expert_counts"),
+                                 _ptr(expert_raw, torch.int32, "expert_raw"),
+                                 _ptr(expert_off, torch.int32, "expert_off"), _ptr(rank_off, torch.int32, "rank_off"),
+                                 _ptr(n_dropped, torch.int32, "n_dropped"), _ptr(ws, what="ws"),
+                                 ws.numel() * ws.element_size(), _stream(stream)), "ep_route_dispatch")
+
+
 def ep_combine(cfg, expert_out, out_scales, out_payload, slot_row, topk_w, y, ws, stream=None):
     _check(lib.ep_combine(ctypes.byref(cfg), _ptr(expert_out, (torch.bfloat16, torch.int8), "expert_out"),
                           _ptr(out_scales, torch.float32, "out_scales"), int(out_payload),
@@ -250,6 +266,12 @@ class EpBuffers:
         ep_dispatch(self.cfg, x, self.topk_idx, self.payload, self.scales, self.row_slot, self.slot_row,
                     self.expert_counts, self.expert_raw, self.expert_off, self.rank_off, self.n_dropped, self.ws,
                     stream)
+
+    def route_dispatch(self, logits, x, stream=None):
+        """ep_route + ep_dispatch as one call (routing fused with the count)."""
+        ep_route_dispatch(self.cfg, logits, x, self.topk_idx, self.topk_w, self.payload, self.scales, self.row_slot,
+                          self.slot_row, self.expert_counts, self.expert_raw, self.expert_off, self.rank_off,
+                          self.n_dropped, self.ws, stream)
 
     def combine(self, expert_out, out_scales=None, stream=None):
         out_payload = EP_PAYLOAD_INT8 if expert_out.dtype == torch.int8 else EP_PAYLOAD_BF16

@@ -10,7 +10,8 @@
 //   y[t,h] = bf16 round-to-nearest-even(acc)
 // The fixed slot order and the explicit fma make the result reproducible.
 //
-// Design: one warp per token in flight, no block-level synchronisation.
+// Design: one warp per work unit in flight (a token, or a slice of a token's
+// row when the batch is short), no block-level synchronisation.
 //   - lanes j < k read slot j's row, weight (and int8 scale) one token ahead;
 //   - a ballot drops the dropped slots and the kept ones are gathered, in
 //     slot order, into registers of every lane (row address, weight, scale),
@@ -93,10 +94,10 @@ __device__ __forceinline__ int gather_group(unsigned& mask, int row, float w, fl
 // One token's chunks with at most NS kept slots (gathered in p/wv/sv): UNR
 // chunks per lane per pass, all NS*UNR loads issued before any arithmetic.
 template <bool INT8, int NS, int UNR>
-__device__ __forceinline__ void combine_token(int nk, int nchunk, int lane, const char* const (&p)[8],
+__device__ __forceinline__ void combine_token(int nk, int cbeg, int nchunk, int lane, const char* const (&p)[8],
                                               const float (&wv)[8], const float (&sv)[8], char* yrow) {
   constexpr int EL = Chunk<INT8>::kElems;
-  for (int c0 = lane; c0 < nchunk; c0 += 32 * UNR) {
+  for (int c0 = cbeg + lane; c0 < nchunk; c0 += 32 * UNR) {
     uint4 v[UNR][NS];
 #pragma unroll
     for (int u = 0; u < UNR; ++u) {
@@ -122,7 +123,7 @@ __device__ __forceinline__ void combine_token(int nk, int nchunk, int lane, cons
 // LOADS = 16-byte loads in flight per lane: a token with few kept slots walks
 // more chunks per pass, so the bytes in flight do not shrink with drops.
 template <bool INT8, int LOADS>
-__global__ void __launch_bounds__(256) combine_kernel(const CombineArgs a) {
+__global__ void __launch_bounds__(256, 2) combine_kernel(const CombineArgs a) {
   constexpr int EL = Chunk<INT8>::kElems;
   const int lane = threadIdx.x & 31;
   const int64_t warp0 = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
@@ -150,14 +151,23 @@ __global__ void __launch_bounds__(256) combine_kernel(const CombineArgs a) {
     }
   };
 
+  // Work unit u = (token u / ns, slice u % ns): slice s covers the 16-byte
+  // chunks [s * cslice, (s + 1) * cslice) of the token's row, so that short
+  // batches still spread over every warp and long ones end with a small tail.
+  const int ns = a.slices;
+  const int cslice = (nchunk + ns - 1) / ns;
+  const int64_t units = static_cast<int64_t>(a.T) * ns;
   int row_n, row;
   float w_n, sc_n, w, sc;
-  load_slot(warp0, row_n, w_n, sc_n);
-  for (int64_t t = warp0; t < a.T; t += nwarps) {
+  load_slot(warp0 / ns, row_n, w_n, sc_n);
+  for (int64_t u = warp0; u < units; u += nwarps) {
+    const int64_t t = u / ns;
+    const int cbeg = static_cast<int>(u - t * ns) * cslice;
+    const int cend = min(nchunk, cbeg + cslice);
     row = row_n;
     w = w_n;
     sc = sc_n;
-    load_slot(t + nwarps, row_n, w_n, sc_n);  // the next token's slots, one token ahead
+    load_slot((u + nwarps) / ns, row_n, w_n, sc_n);  // the next unit's slots, one unit ahead
 
     const unsigned kept = __ballot_sync(kFull, row >= 0);
     const int nk = __popc(kept);
@@ -168,15 +178,15 @@ __global__ void __launch_bounds__(256) combine_kernel(const CombineArgs a) {
       unsigned m = kept;
       gather_group<INT8>(m, row, w, sc, base, row_bytes, p, wv, sv);
       if (nk <= 2)
-        combine_token<INT8, 2, LOADS / 2>(nk, nchunk, lane, p, wv, sv, yrow);
+        combine_token<INT8, 2, LOADS / 2>(nk, cbeg, cend, lane, p, wv, sv, yrow);
       else if (nk <= 4)
-        combine_token<INT8, 4, LOADS / 4>(nk, nchunk, lane, p, wv, sv, yrow);
+        combine_token<INT8, 4, LOADS / 4>(nk, cbeg, cend, lane, p, wv, sv, yrow);
       else
-        combine_token<INT8, 8, LOADS / 8>(nk, nchunk, lane, p, wv, sv, yrow);
+        combine_token<INT8, 8, LOADS / 8>(nk, cbeg, cend, lane, p, wv, sv, yrow);
     } else {
       // k > 8 with more than 8 kept slots: groups of 8 per chunk, slot order.
       // The loop bound is warp-uniform: the gathers shuffle across all lanes.
-      for (int c0 = 0; c0 < nchunk; c0 += 32) {
+      for (int c0 = cbeg; c0 < cend; c0 += 32) {
         const int c = c0 + lane;
         float acc[EL];
 #pragma unroll
@@ -187,12 +197,12 @@ __global__ void __launch_bounds__(256) combine_kernel(const CombineArgs a) {
           uint4 v[8];
 #pragma unroll
           for (int i = 0; i < 8; ++i)
-            v[i] = (i < n && c < nchunk) ? ld_stream_v4(p[i] + 16 * static_cast<int64_t>(c)) : make_uint4(0, 0, 0, 0);
+            v[i] = (i < n && c < cend) ? ld_stream_v4(p[i] + 16 * static_cast<int64_t>(c)) : make_uint4(0, 0, 0, 0);
 #pragma unroll
           for (int i = 0; i < 8; ++i)
             if (i < n) fma_chunk<INT8>(acc, v[i], wv[i], sv[i]);
         }
-        if (c < nchunk) store_bf16<EL>(yrow + 2 * static_cast<int64_t>(c) * EL, acc);
+        if (c < cend) store_bf16<EL>(yrow + 2 * static_cast<int64_t>(c) * EL, acc);
       }
     }
   }
@@ -231,11 +241,19 @@ __global__ void __launch_bounds__(1024) quantize_rows_kernel(const void* __restr
 int g_occ_combine[4][64];
 
 template <bool INT8, int LOADS>
-cudaError_t launch_combine_t(const CombineArgs& a, int sms, int* cache, cudaStream_t s) {
+cudaError_t launch_combine_t(CombineArgs a, int sms, int* cache, cudaStream_t s) {
   constexpr int kBlock = 256;
   const int per_sm = resident_ctas(combine_kernel<INT8, LOADS>, kBlock, 0, cache);
-  const int64_t warps_needed = a.T;
-  const int64_t blocks_needed = (warps_needed + kBlock / 32 - 1) / (kBlock / 32);
+  const int64_t warps = static_cast<int64_t>(sms) * per_sm * (kBlock / 32);
+  // Slices per token: enough work units for about eight per warp, but no
+  // slice shorter than one pass of the warp over its chunks.
+  const int nchunk = INT8 ? a.H / 16 : a.H / 8;
+  const int min_slice = 32 * (LOADS / 8);
+  int ns = static_cast<int>((8 * warps + a.T - 1) / a.T);
+  const int max_ns = nchunk / min_slice > 1 ? nchunk / min_slice : 1;
+  a.slices = ns < 1 ? 1 : (ns > max_ns ? max_ns : ns);
+  const int64_t units = static_cast<int64_t>(a.T) * a.slices;
+  const int64_t blocks_needed = (units + kBlock / 32 - 1) / (kBlock / 32);
   const int64_t want = static_cast<int64_t>(sms) * per_sm;
   const int grid = static_cast<int>(blocks_needed < want ? blocks_needed : want);
   return launch_pdl(combine_kernel<INT8, LOADS>, grid, kBlock, 0, s, a);

@@ -428,15 +428,20 @@ cudaError_t launch_dispatch(const DispatchArgs& a, int sms, cudaStream_t s) {
   err = launch_pdl(count_kernel, a.ntiles > 0 ? a.ntiles : 1, cblock, static_cast<size_t>(smem), s, a.topk_idx, a.T,
                    a.E, a.k, a.tile, a.ntiles, a.tile_counts, a.lrank, a.status, a.ticket);
   if (err != cudaSuccess) return err;
-  err = launch_pdl(scan_kernel, a.E, 256, 0, s, a.tile_counts, a.E, a.R, a.ntiles, a.cap, a.tile_base, a.expert_counts,
+  return launch_scan_scatter(a, sms, s);
+}
+
+cudaError_t launch_scan_scatter(const DispatchArgs& a, int sms, cudaStream_t s) {
+  cudaError_t err = launch_pdl(scan_kernel, a.E, 256, 0, s, a.tile_counts, a.E, a.R, a.ntiles, a.cap, a.tile_base, a.expert_counts,
                    a.expert_raw, a.expert_off, a.rank_off, a.n_dropped, a.kept, a.dropped, a.ticket);
   if (err != cudaSuccess) return err;
   if (a.T == 0) return cudaSuccess;
 
   const int tile_log2 = __builtin_ctz(static_cast<unsigned>(a.tile));
   if (a.int8) {
-    // two 16-element groups per thread: H/32 threads per token, >= 32 >= k
-    const int block = ((a.H / 32 + 31) / 32) * 32;
+    // two 16-element groups per thread: ceil(H/32) threads per token, rounded
+    // up to whole warps (>= 32 >= k)
+    const int block = (((a.H / 16 + 1) / 2 + 31) / 32) * 32;
     const bool v8 = (reinterpret_cast<uintptr_t>(a.x) & 31u) == 0;  // rows are then 32-byte aligned too
     static int occ[2][16][64];  // per load width, block size / 32, device
     const int per_sm = v8 ? resident_ctas(scatter_int8_kernel<true>, block, 0, occ[1][block / 32 - 1])

@@ -63,6 +63,62 @@ int64_t max_rows_of(const ep_config_t* c) {
 
 ep_status_t from_cuda(cudaError_t e) { return e == cudaSuccess ? EP_OK : EP_ERR_CUDA; }
 
+// Checks the dispatch arguments (before any launch) and fills the kernel
+// arguments, with the workspace carved into its regions.
+ep_status_t prepare_dispatch(const ep_config_t* cfg, const void* x, const int32_t* topk_idx, void* payload,
+                             float* scales, int32_t* row_slot, int32_t* slot_row, int32_t* expert_counts,
+                             int32_t* expert_raw, int32_t* expert_off, int32_t* rank_off, int32_t* n_dropped,
+                             void* ws, size_t ws_bytes, ep::DispatchArgs* out, int* sms_out) {
+  if (!config_ok(cfg)) return EP_ERR_INVALID_ARG;
+  const bool int8 = cfg->payload == EP_PAYLOAD_INT8;
+  if (!expert_counts || !expert_off || !rank_off || !n_dropped) return EP_ERR_INVALID_ARG;
+  if (cfg->T > 0) {
+    if (!x || !topk_idx || !payload || !row_slot || !slot_row) return EP_ERR_INVALID_ARG;
+    if (int8 && !scales) return EP_ERR_INVALID_ARG;
+    if (!aligned(x, 16) || !aligned(payload, 16)) return EP_ERR_INVALID_ARG;
+  }
+  if (!aligned(topk_idx, 4) || !aligned(row_slot, 4) || !aligned(slot_row, 4) || !aligned(expert_counts, 4) ||
+      !aligned(expert_raw, 4) || !aligned(expert_off, 4) || !aligned(rank_off, 4) || !aligned(n_dropped, 4) ||
+      !aligned(scales, 4))
+    return EP_ERR_INVALID_ARG;
+  const ep::WsLayout L = ep::ws_layout(cfg->T, cfg->E, cfg->k);
+  if (ws == nullptr || ws_bytes < L.total || !aligned(ws, 256)) return EP_ERR_WORKSPACE;
+  const int sms = current_sm_count();
+  if (sms <= 0) return EP_ERR_CUDA;
+
+  char* w = static_cast<char*>(ws);
+  ep::DispatchArgs& a = *out;
+  a.T = cfg->T;
+  a.H = cfg->H;
+  a.E = cfg->E;
+  a.k = cfg->k;
+  a.R = cfg->R;
+  a.cap = capacity_of(cfg);
+  a.int8 = int8 ? 1 : 0;
+  a.x = x;
+  a.topk_idx = topk_idx;
+  a.payload = payload;
+  a.scales = scales;
+  a.row_slot = row_slot;
+  a.slot_row = slot_row;
+  a.expert_counts = expert_counts;
+  a.expert_raw = expert_raw;
+  a.expert_off = expert_off;
+  a.rank_off = rank_off;
+  a.n_dropped = n_dropped;
+  a.status = reinterpret_cast<uint32_t*>(w + L.status_off);
+  a.ticket = reinterpret_cast<uint32_t*>(w + L.ticket_off);
+  a.kept = reinterpret_cast<int32_t*>(w + L.kept_off);
+  a.dropped = reinterpret_cast<int32_t*>(w + L.drop_off);
+  a.tile_counts = reinterpret_cast<int32_t*>(w + L.tile_counts_off);
+  a.tile_base = reinterpret_cast<int32_t*>(w + L.tile_base_off);
+  a.lrank = reinterpret_cast<int32_t*>(w + L.lrank_off);
+  a.tile = L.tile;
+  a.ntiles = L.ntiles;
+  *sms_out = sms;
+  return EP_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -115,53 +171,44 @@ ep_status_t ep_dispatch(const ep_config_t* cfg, const void* x, const int32_t* to
                         float* scales, int32_t* row_slot, int32_t* slot_row, int32_t* expert_counts,
                         int32_t* expert_raw, int32_t* expert_off, int32_t* rank_off, int32_t* n_dropped,
                         void* ws, size_t ws_bytes, cudaStream_t stream) {
-  if (!config_ok(cfg)) return EP_ERR_INVALID_ARG;
-  const bool int8 = cfg->payload == EP_PAYLOAD_INT8;
-  if (!expert_counts || !expert_off || !rank_off || !n_dropped) return EP_ERR_INVALID_ARG;
-  if (cfg->T > 0) {
-    if (!x || !topk_idx || !payload || !row_slot || !slot_row) return EP_ERR_INVALID_ARG;
-    if (int8 && !scales) return EP_ERR_INVALID_ARG;
-    if (!aligned(x, 16) || !aligned(payload, 16)) return EP_ERR_INVALID_ARG;
-  }
-  if (!aligned(topk_idx, 4) || !aligned(row_slot, 4) || !aligned(slot_row, 4) || !aligned(expert_counts, 4) ||
-      !aligned(expert_raw, 4) || !aligned(expert_off, 4) || !aligned(rank_off, 4) || !aligned(n_dropped, 4) ||
-      !aligned(scales, 4))
-    return EP_ERR_INVALID_ARG;
-  const ep::WsLayout L = ep::ws_layout(cfg->T, cfg->E, cfg->k);
-  if (ws == nullptr || ws_bytes < L.total || !aligned(ws, 256)) return EP_ERR_WORKSPACE;
-  const int sms = current_sm_count();
-  if (sms <= 0) return EP_ERR_CUDA;
-
-  char* w = static_cast<char*>(ws);
   ep::DispatchArgs a;
-  a.T = cfg->T;
-  a.H = cfg->H;
-  a.E = cfg->E;
-  a.k = cfg->k;
-  a.R = cfg->R;
-  a.cap = capacity_of(cfg);
-  a.int8 = int8 ? 1 : 0;
-  a.x = x;
-  a.topk_idx = topk_idx;
-  a.payload = payload;
-  a.scales = scales;
-  a.row_slot = row_slot;
-  a.slot_row = slot_row;
-  a.expert_counts = expert_counts;
-  a.expert_raw = expert_raw;
-  a.expert_off = expert_off;
-  a.rank_off = rank_off;
-  a.n_dropped = n_dropped;
-  a.status = reinterpret_cast<uint32_t*>(w + L.status_off);
-  a.ticket = reinterpret_cast<uint32_t*>(w + L.ticket_off);
-  a.kept = reinterpret_cast<int32_t*>(w + L.kept_off);
-  a.dropped = reinterpret_cast<int32_t*>(w + L.drop_off);
-  a.tile_counts = reinterpret_cast<int32_t*>(w + L.tile_counts_off);
-  a.tile_base = reinterpret_cast<int32_t*>(w + L.tile_base_off);
-  a.lrank = reinterpret_cast<int32_t*>(w + L.lrank_off);
-  a.tile = L.tile;
-  a.ntiles = L.ntiles;
+  int sms = 0;
+  const ep_status_t st = prepare_dispatch(cfg, x, topk_idx, payload, scales, row_slot, slot_row, expert_counts,
+                                          expert_raw, expert_off, rank_off, n_dropped, ws, ws_bytes, &a, &sms);
+  if (st != EP_OK) return st;
   return from_cuda(ep::launch_dispatch(a, sms, stream));
+}
+
+ep_status_t ep_route_dispatch(const ep_config_t* cfg, const float* logits, const void* x, int32_t* topk_idx,
+                              float* topk_w, void* payload, float* scales, int32_t* row_slot, int32_t* slot_row,
+                              int32_t* expert_counts, int32_t* expert_raw, int32_t* expert_off, int32_t* rank_off,
+                              int32_t* n_dropped, void* ws, size_t ws_bytes, cudaStream_t stream) {
+  if (!config_ok(cfg)) return EP_ERR_INVALID_ARG;
+  if (cfg->T > 0) {
+    if (!logits || !topk_idx || !topk_w) return EP_ERR_INVALID_ARG;
+    if (!aligned(logits, 16) || !aligned(topk_w, 4)) return EP_ERR_INVALID_ARG;
+  }
+  ep::DispatchArgs a;
+  int sms = 0;
+  const ep_status_t st = prepare_dispatch(cfg, x, topk_idx, payload, scales, row_slot, slot_row, expert_counts,
+                                          expert_raw, expert_off, rank_off, n_dropped, ws, ws_bytes, &a, &sms);
+  if (st != EP_OK) return st;
+  ep::RouteCountArgs r;
+  r.logits = logits;
+  r.T = cfg->T;
+  r.E = cfg->E;
+  r.k = cfg->k;
+  r.renorm = cfg->renormalize;
+  r.tile = a.tile;
+  r.ntiles = a.ntiles;
+  r.topk_idx = topk_idx;
+  r.topk_w = topk_w;
+  r.tile_counts = a.tile_counts;
+  r.lrank = a.lrank;
+  r.ticket = a.ticket;
+  const cudaError_t err = ep::launch_route_count(r, stream);
+  if (err != cudaSuccess) return EP_ERR_CUDA;
+  return from_cuda(ep::launch_scan_scatter(a, sms, stream));
 }
 
 ep_status_t ep_combine(const ep_config_t* cfg, const void* expert_out, const float* out_scales,

@@ -100,10 +100,26 @@ struct DispatchArgs {
   int tile, ntiles;
 };
 
+// ep_dispatch: count kernel, then scan and scatter.
 cudaError_t launch_dispatch(const DispatchArgs& a, int sms, cudaStream_t s);
+// The scan and the scatter alone, once tile_counts / lrank are written (by
+// the count kernel or the fused route+count kernel) and the ticket is clear.
+cudaError_t launch_scan_scatter(const DispatchArgs& a, int sms, cudaStream_t s);
+
+// Routing fused with the dispatch's per-tile count (ep_route_dispatch).
+struct RouteCountArgs {
+  const float* logits;
+  int T, E, k, renorm, tile, ntiles;
+  int32_t* topk_idx;
+  float* topk_w;
+  int32_t *tile_counts, *lrank;
+  uint32_t* ticket;
+};
+cudaError_t launch_route_count(const RouteCountArgs& r, cudaStream_t s);
 
 struct CombineArgs {
   int T, H, k, int8_out;
+  int slices;  // work units per token (set by the launcher)
   int64_t max_rows;
   const void* expert_out;
   const float* out_scales;

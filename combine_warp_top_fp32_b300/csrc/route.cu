@@ -18,8 +18,9 @@
 //     max is always its first key; with several tokens per warp the group max
 //     is a __shfl_xor_sync butterfly;
 //   - softmax denominator: exp(l - l_max) with the subtraction's rounding
-//     error carried into the exponential, summed with compensated (Neumaier /
-//     TwoSum) arithmetic, so the weight stays within 1e-6 of the exact value.
+//     error carried into the exponential (exp_shifted_term), summed with
+//     compensated (TwoSum) arithmetic; each chosen expert's numerator uses
+//     expf, so the weight stays within 1e-6 of the exact value.
 #include "ep_internal.h"
 
 namespace ep {
@@ -86,13 +87,35 @@ __device__ __forceinline__ float exp_shifted(float v, float m) {
   return __fmaf_rn(e, err, e);
 }
 
-// Neumaier compensated accumulation of x into (s, c).
+// exp(v - m) for a softmax denominator term, built on the hardware base-2
+// exponential: v - m = d + err exactly (TwoSum); (d + err) * log2(e) is
+// carried as p + c with p = fl(d * L1), L1 = log2(e) rounded to fp32, and c
+// collecting the product's exact rounding error (fma), d * (log2(e) - L1) and
+// err * L1; then 2^(p + c) ~= 2^p * (1 + c * ln 2). Relative error about 3.4
+// fp32 ulp (measured over d in [-87, 0] against a double-precision exp),
+// against 2.6 for expf. Results below 2^-126 flush to zero, which changes a
+// sum that is at least 1 by less than 2^-126 per term.
+__device__ __forceinline__ float exp_shifted_term(float v, float m) {
+  constexpr float kLog2eHi = 1.44269502162933349609375f;  // fp32 nearest to log2(e)
+  constexpr float kLog2eLo = 1.925963033500011e-08f;      // log2(e) - kLog2eHi
+  constexpr float kLn2 = 0.693147180559945309f;
+  const float nm = -m;
+  const float d = __fadd_rn(v, nm);
+  const float bb = __fsub_rn(d, v);
+  const float err = __fadd_rn(__fsub_rn(v, __fsub_rn(d, bb)), __fsub_rn(nm, bb));
+  const float p = __fmul_rn(d, kLog2eHi);
+  const float c = __fmaf_rn(err, kLog2eHi, __fmaf_rn(d, kLog2eLo, __fmaf_rn(d, kLog2eHi, -p)));
+  float r;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(p));
+  return __fmaf_rn(r, __fmul_rn(c, kLn2), r);
+}
+
+// Compensated accumulation of x into (s, c): TwoSum gives the exact rounding
+// error of s + x, which is added to the running correction c.
 __device__ __forceinline__ void comp_add(float& s, float& c, float x) {
   const float t = __fadd_rn(s, x);
-  if (fabsf(s) >= fabsf(x))
-    c = __fadd_rn(c, __fadd_rn(__fsub_rn(s, t), x));
-  else
-    c = __fadd_rn(c, __fadd_rn(__fsub_rn(x, t), s));
+  const float bb = __fsub_rn(t, s);
+  c = __fadd_rn(c, __fadd_rn(__fsub_rn(s, __fsub_rn(t, bb)), __fsub_rn(x, bb)));
   s = t;
 }
 
@@ -109,6 +132,147 @@ __device__ __forceinline__ float group_comp_sum(float s, float c, int L) {
     s = t;
   }
   return __fadd_rn(s, c);
+}
+
+// Routes one token per L-lane group: on return lanes sub < k of the group
+// hold slot sub's expert id (*e_out) and weight (*w_out). All 32 lanes of the
+// warp must call it together (warp-wide reductions).
+template <int VPL, bool VEC4>
+__device__ __forceinline__ void route_token(const float* __restrict__ logits, int64_t t, bool active, int E, int k,
+                                            int L, int sub, int renorm, int* e_out, float* w_out) {
+  const float* row = logits + (active ? t : 0) * static_cast<int64_t>(E);
+
+  float val[VPL];
+  uint64_t key[VPL];
+  if constexpr (VEC4) {
+    // lane `sub` holds experts 4*sub + 128*i + c, i < VPL/4, c < 4
+#pragma unroll
+    for (int i = 0; i < VPL / 4; ++i) {
+      const int e0 = 4 * sub + 128 * i;
+      float4 f = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (active) f = __ldg(reinterpret_cast<const float4*>(row + e0));
+      val[4 * i + 0] = f.x;
+      val[4 * i + 1] = f.y;
+      val[4 * i + 2] = f.z;
+      val[4 * i + 3] = f.w;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) key[4 * i + c] = active ? make_key(val[4 * i + c], e0 + c) : 0ull;
+    }
+  } else {
+    // lane `sub` holds experts sub + L*i
+#pragma unroll
+    for (int i = 0; i < VPL; ++i) {
+      const int e = sub + L * i;
+      const bool ok = active && e < E;
+      val[i] = ok ? __ldg(row + e) : 0.f;
+      key[i] = ok ? make_key(val[i], e) : 0ull;  // 0 is below every real key
+    }
+  }
+
+  // k rounds of group argmax; lane j of the group keeps slot j.
+  int my_e = 0;
+  float my_v = 0.f;
+  float l_max = 0.f;
+  if (L == 32 && VPL <= 8) {
+    // One token per warp, each lane's keys sorted once (largest first):
+    // every round the lanes offer their head key; redux.sync max over the
+    // value bits finds the largest logit, redux.sync min over the ids of
+    // the lanes offering it breaks the tie toward the lower expert id, and
+    // the winning lane drops its head (a shift of its sorted list).
+    sort_desc<VPL>(key);
+    uint32_t my_bits = 0, max_bits = 0;
+    for (int r = 0; r < k; ++r) {
+      const uint32_t hv = static_cast<uint32_t>(key[0] >> 32);
+      const uint32_t gmax = __reduce_max_sync(0xffffffffu, hv);
+      const uint32_t cand = (hv == gmax) ? 0xffffffffu - static_cast<uint32_t>(key[0]) : 0xffffffffu;
+      const uint32_t win = __reduce_min_sync(0xffffffffu, cand);
+      if (r == 0) max_bits = gmax;
+      if (sub == r) {
+        my_e = static_cast<int>(win);
+        my_bits = gmax;
+      }
+      if (cand == win) {
+#pragma unroll
+        for (int i = 0; i + 1 < VPL; ++i) key[i] = key[i + 1];
+        key[VPL - 1] = 0ull;  // 0 is below every real key
+      }
+    }
+    l_max = key_value(static_cast<uint64_t>(max_bits) << 32);
+    my_v = key_value(static_cast<uint64_t>(my_bits) << 32);
+  } else if (L == 32) {
+    // One token per warp: two single-instruction warp reductions per round.
+    // redux.sync max over the order-preserving value bits finds the largest
+    // logit, redux.sync min over the ids of the lanes holding it breaks the
+    // tie toward the lower expert id. Within a lane the ids grow with i, so
+    // a strict '>' keeps the lowest id among the lane's equal values.
+    uint32_t ob[VPL];
+#pragma unroll
+    for (int i = 0; i < VPL; ++i) ob[i] = static_cast<uint32_t>(key[i] >> 32);
+    for (int r = 0; r < k; ++r) {
+      uint32_t bv = ob[0];
+      int bi = 0;
+#pragma unroll
+      for (int i = 1; i < VPL; ++i)
+        if (ob[i] > bv) {
+          bv = ob[i];
+          bi = i;
+        }
+      const uint32_t gmax = __reduce_max_sync(0xffffffffu, bv);
+      uint32_t my_id = 0xffffffffu;
+#pragma unroll
+      for (int i = 0; i < VPL; ++i)
+        if (i == bi) my_id = 0xffffffffu - static_cast<uint32_t>(key[i]);
+      const uint32_t cand = (bv == gmax) ? my_id : 0xffffffffu;
+      const uint32_t win = __reduce_min_sync(0xffffffffu, cand);
+      const float v = key_value(static_cast<uint64_t>(gmax) << 32);
+      if (r == 0) l_max = v;
+      if (sub == r) {
+        my_e = static_cast<int>(win);
+        my_v = v;
+      }
+      if (cand == win) {
+#pragma unroll
+        for (int i = 0; i < VPL; ++i)
+          if (i == bi) ob[i] = 0u;  // 0 is below every real value
+      }
+    }
+  } else {
+    for (int r = 0; r < k; ++r) {
+      uint64_t best = key[0];
+#pragma unroll
+      for (int i = 1; i < VPL; ++i) best = umax64(best, key[i]);
+      for (int o = L >> 1; o > 0; o >>= 1) best = umax64(best, __shfl_xor_sync(0xffffffffu, best, o));
+      const float v = key_value(best);
+      if (r == 0) l_max = v;
+      if (sub == r) {
+        my_e = key_expert(best);
+        my_v = v;
+      }
+#pragma unroll
+      for (int i = 0; i < VPL; ++i)
+        if (key[i] == best) key[i] = 0ull;
+    }
+  }
+
+  // softmax denominator: all E experts, or the k chosen when renormalising
+  float s = 0.f, c = 0.f;
+  if (renorm) {
+    if (sub < k) s = exp_shifted_term(my_v, l_max);
+  } else {
+#pragma unroll
+    for (int i = 0; i < VPL; ++i) {
+      bool ok;
+      if constexpr (VEC4)
+        ok = active;
+      else
+        ok = active && (sub + L * i) < E;
+      if (ok) comp_add(s, c, exp_shifted_term(val[i], l_max));
+    }
+  }
+  const float denom = group_comp_sum(s, c, L);
+
+  *e_out = my_e;
+  *w_out = __fdiv_rn(exp_shifted(my_v, l_max), denom);
 }
 
 template <int VPL, bool VEC4>
@@ -128,140 +292,76 @@ __global__ void __launch_bounds__(256) route_topk_kernel(const float* __restrict
   for (int64_t tb = warp_id * groups_per_warp; tb < T; tb += n_warps * groups_per_warp) {
     const int64_t t = tb + grp;
     const bool active = t < T;
-    const float* row = logits + (active ? t : 0) * static_cast<int64_t>(E);
-
-    float val[VPL];
-    uint64_t key[VPL];
-    if constexpr (VEC4) {
-      // lane `sub` holds experts 4*sub + 128*i + c, i < VPL/4, c < 4
-#pragma unroll
-      for (int i = 0; i < VPL / 4; ++i) {
-        const int e0 = 4 * sub + 128 * i;
-        float4 f = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (active) f = __ldg(reinterpret_cast<const float4*>(row + e0));
-        val[4 * i + 0] = f.x;
-        val[4 * i + 1] = f.y;
-        val[4 * i + 2] = f.z;
-        val[4 * i + 3] = f.w;
-#pragma unroll
-        for (int c = 0; c < 4; ++c) key[4 * i + c] = active ? make_key(val[4 * i + c], e0 + c) : 0ull;
-      }
-    } else {
-      // lane `sub` holds experts sub + L*i
-#pragma unroll
-      for (int i = 0; i < VPL; ++i) {
-        const int e = sub + L * i;
-        const bool ok = active && e < E;
-        val[i] = ok ? __ldg(row + e) : 0.f;
-        key[i] = ok ? make_key(val[i], e) : 0ull;  // 0 is below every real key
-      }
-    }
-
-    // k rounds of group argmax; lane j of the group keeps slot j.
-    int my_e = 0;
-    float my_v = 0.f;
-    float l_max = 0.f;
-    if (L == 32 && VPL <= 8) {
-      // One token per warp, each lane's keys sorted once (largest first):
-      // every round the lanes offer their head key; redux.sync max over the
-      // value bits finds the largest logit, redux.sync min over the ids of
-      // the lanes offering it breaks the tie toward the lower expert id, and
-      // the winning lane drops its head (a shift of its sorted list).
-      sort_desc<VPL>(key);
-      for (int r = 0; r < k; ++r) {
-        const uint32_t hv = static_cast<uint32_t>(key[0] >> 32);
-        const uint32_t gmax = __reduce_max_sync(0xffffffffu, hv);
-        const uint32_t cand = (hv == gmax) ? 0xffffffffu - static_cast<uint32_t>(key[0]) : 0xffffffffu;
-        const uint32_t win = __reduce_min_sync(0xffffffffu, cand);
-        const float v = key_value(static_cast<uint64_t>(gmax) << 32);
-        if (r == 0) l_max = v;
-        if (sub == r) {
-          my_e = static_cast<int>(win);
-          my_v = v;
-        }
-        if (cand == win) {
-#pragma unroll
-          for (int i = 0; i + 1 < VPL; ++i) key[i] = key[i + 1];
-          key[VPL - 1] = 0ull;  // 0 is below every real key
-        }
-      }
-    } else if (L == 32) {
-      // One token per warp: two single-instruction warp reductions per round.
-      // redux.sync max over the order-preserving value bits finds the largest
-      // logit, redux.sync min over the ids of the lanes holding it breaks the
-      // tie toward the lower expert id. Within a lane the ids grow with i, so
-      // a strict '>' keeps the lowest id among the lane's equal values.
-      uint32_t ob[VPL];
-#pragma unroll
-      for (int i = 0; i < VPL; ++i) ob[i] = static_cast<uint32_t>(key[i] >> 32);
-      for (int r = 0; r < k; ++r) {
-        uint32_t bv = ob[0];
-        int bi = 0;
-#pragma unroll
-        for (int i = 1; i < VPL; ++i)
-          if (ob[i] > bv) {
-            bv = ob[i];
-            bi = i;
-          }
-        const uint32_t gmax = __reduce_max_sync(0xffffffffu, bv);
-        uint32_t my_id = 0xffffffffu;
-#pragma unroll
-        for (int i = 0; i < VPL; ++i)
-          if (i == bi) my_id = 0xffffffffu - static_cast<uint32_t>(key[i]);
-        const uint32_t cand = (bv == gmax) ? my_id : 0xffffffffu;
-        const uint32_t win = __reduce_min_sync(0xffffffffu, cand);
-        const float v = key_value(static_cast<uint64_t>(gmax) << 32);
-        if (r == 0) l_max = v;
-        if (sub == r) {
-          my_e = static_cast<int>(win);
-          my_v = v;
-        }
-        if (cand == win) {
-#pragma unroll
-          for (int i = 0; i < VPL; ++i)
-            if (i == bi) ob[i] = 0u;  // 0 is below every real value
-        }
-      }
-    } else {
-      for (int r = 0; r < k; ++r) {
-        uint64_t best = key[0];
-#pragma unroll
-        for (int i = 1; i < VPL; ++i) best = umax64(best, key[i]);
-        for (int o = L >> 1; o > 0; o >>= 1) best = umax64(best, __shfl_xor_sync(0xffffffffu, best, o));
-        const float v = key_value(best);
-        if (r == 0) l_max = v;
-        if (sub == r) {
-          my_e = key_expert(best);
-          my_v = v;
-        }
-#pragma unroll
-        for (int i = 0; i < VPL; ++i)
-          if (key[i] == best) key[i] = 0ull;
-      }
-    }
-
-    // softmax denominator: all E experts, or the k chosen when renormalising
-    float s = 0.f, c = 0.f;
-    if (renorm) {
-      if (sub < k) s = exp_shifted(my_v, l_max);
-    } else {
-#pragma unroll
-      for (int i = 0; i < VPL; ++i) {
-        bool ok;
-        if constexpr (VEC4)
-          ok = active;
-        else
-          ok = active && (sub + L * i) < E;
-        if (ok) comp_add(s, c, exp_shifted(val[i], l_max));
-      }
-    }
-    const float denom = group_comp_sum(s, c, L);
-
+    int e;
+    float w;
+    route_token<VPL, VEC4>(logits, t, active, E, k, L, sub, renorm, &e, &w);
     if (active && sub < k) {
-      const float num = exp_shifted(my_v, l_max);
-      topk_idx[t * k + sub] = my_e;
-      topk_w[t * k + sub] = __fdiv_rn(num, denom);
+      topk_idx[t * k + sub] = e;
+      topk_w[t * k + sub] = w;
     }
+  }
+}
+
+// Routing fused with the per-tile count of the dispatch (the ThunderEP
+// article's §5.2 suggestion to bucket by destination while routing): CTA b
+// routes the tokens of tile b = [b*tile, (b+1)*tile), writes their slots,
+// and builds the tile's per-expert bit masks in shared memory, from which it
+// writes the tile's count per expert and each pair's rank within the tile in
+// token order (the same tile_counts / lrank as the dispatch's count kernel).
+template <int VPL, bool VEC4>
+__global__ void __launch_bounds__(VPL >= 16 ? 256 : 512) route_count_kernel(
+    const float* __restrict__ logits, int T, int E, int k, int lanes_log2, int renorm, int tile, int ntiles,
+    int32_t* __restrict__ topk_idx, float* __restrict__ topk_w, int32_t* __restrict__ tile_counts,
+    int32_t* __restrict__ lrank, uint32_t* ticket) {
+  extern __shared__ uint32_t smem[];
+  const int L = 1 << lanes_log2;
+  const int lane = threadIdx.x & 31;
+  const int sub = lane & (L - 1);
+  const int groups_per_warp = 32 >> lanes_log2;
+  const int grp = lane >> lanes_log2;
+  const int warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  const int TW = tile >> 5;
+  uint32_t* mask = smem;          // [E][TW] bit b of word w: token 32*w+b of the tile chose e
+  uint32_t* pre = smem + E * TW;  // [E][TW] set bits of e in the words before w
+  const int b = blockIdx.x;
+  const int64_t t0 = static_cast<int64_t>(b) * tile;
+  const int nt = static_cast<int>(min(static_cast<int64_t>(tile), T - t0));
+  for (int i = threadIdx.x; i < E * TW; i += blockDim.x) mask[i] = 0u;
+  pdl_wait();  // the logits may come from the kernel before this one
+  pdl_launch_dependents();
+  if (b == 0 && threadIdx.x == 0) *ticket = 0u;  // the scan that follows counts its CTAs from 0
+  __syncthreads();
+  if (nt <= 0) return;  // an empty batch: only the ticket
+
+  for (int tl0 = warp * groups_per_warp; tl0 < nt; tl0 += nw * groups_per_warp) {
+    const int tl = tl0 + grp;
+    const bool active = tl < nt;
+    const int64_t t = t0 + tl;
+    int e;
+    float w;
+    route_token<VPL, VEC4>(logits, t, active, E, k, L, sub, renorm, &e, &w);
+    if (active && sub < k) {
+      topk_idx[t * k + sub] = e;
+      topk_w[t * k + sub] = w;
+      atomicOr(&mask[e * TW + (tl >> 5)], 1u << (tl & 31));
+    }
+  }
+  __syncthreads();
+
+  for (int e = warp; e < E; e += nw) {
+    const int c = lane < TW ? __popc(mask[e * TW + lane]) : 0;
+    const int incl = warp_inclusive_scan(c);
+    if (lane < TW) pre[e * TW + lane] = static_cast<uint32_t>(incl - c);
+    if (lane == 31) tile_counts[static_cast<int64_t>(e) * ntiles + b] = incl;
+  }
+  __syncthreads();
+
+  const int64_t base = t0 * k;
+  for (int p = threadIdx.x; p < nt * k; p += blockDim.x) {
+    const int e = topk_idx[base + p];  // written above by this CTA
+    const int tl = p / k;
+    const int w = tl >> 5;
+    lrank[base + p] = static_cast<int>(pre[e * TW + w]) + __popc(mask[e * TW + w] & ((1u << (tl & 31)) - 1u));
   }
 }
 
@@ -275,6 +375,26 @@ cudaError_t launch_route_t(const float* logits, int T, int E, int k, int lanes_l
   const int64_t cap_blocks = static_cast<int64_t>(sms) * resident_ctas(route_topk_kernel<VPL, VEC4>, 256, 0, occ);
   const int grid = static_cast<int>(blocks_needed < cap_blocks ? blocks_needed : cap_blocks);
   return launch_pdl(route_topk_kernel<VPL, VEC4>, grid, 256, 0, s, logits, T, E, k, lanes_log2, renorm, idx, w);
+}
+
+template <int VPL, bool VEC4>
+cudaError_t launch_route_count_t(const RouteCountArgs& r, int lanes_log2, cudaStream_t s) {
+  constexpr int kBlock = VPL >= 16 ? 256 : 512;
+  static int smem_set[64];  // per device: largest dynamic shared size already allowed
+  const int smem = 2 * r.E * (r.tile / 32) * static_cast<int>(sizeof(uint32_t));
+  if (smem > 48 * 1024) {
+    int dev = 0;
+    cudaError_t err = cudaGetDevice(&dev);
+    if (err != cudaSuccess) return err;
+    if (dev >= 64 || smem_set[dev] < smem) {
+      err = cudaFuncSetAttribute(route_count_kernel<VPL, VEC4>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+      if (err != cudaSuccess) return err;
+      if (dev < 64) smem_set[dev] = smem;
+    }
+  }
+  return launch_pdl(route_count_kernel<VPL, VEC4>, r.ntiles > 0 ? r.ntiles : 1, kBlock, static_cast<size_t>(smem),
+                    s, r.logits, r.T, r.E, r.k, lanes_log2, r.renorm, r.tile, r.ntiles, r.topk_idx, r.topk_w,
+                    r.tile_counts, r.lrank, r.ticket);
 }
 
 }  // namespace
@@ -302,6 +422,33 @@ cudaError_t launch_route(const float* logits, int T, int E, int k, int renorm, i
   if (vpl <= 8) return launch_route_t<8, false>(logits, T, E, k, lanes_log2, renorm, idx, w, sms, s);
   if (vpl <= 16) return launch_route_t<16, false>(logits, T, E, k, lanes_log2, renorm, idx, w, sms, s);
   return launch_route_t<32, false>(logits, T, E, k, lanes_log2, renorm, idx, w, sms, s);
+}
+
+}  // namespace ep
+
+namespace ep {
+
+cudaError_t launch_route_count(const RouteCountArgs& r, cudaStream_t s) {
+  int lanes_log2 = 0;
+  while ((1 << lanes_log2) < r.E && lanes_log2 < 5) ++lanes_log2;
+  const int L = 1 << lanes_log2;
+  const int vpl = (r.E + L - 1) / L;
+  const bool vec4 = (L == 32) && (r.E % 128 == 0);
+  if (vec4) {
+    switch (vpl) {
+      case 4: return launch_route_count_t<4, true>(r, lanes_log2, s);
+      case 8: return launch_route_count_t<8, true>(r, lanes_log2, s);
+      case 16: return launch_route_count_t<16, true>(r, lanes_log2, s);
+      case 32: return launch_route_count_t<32, true>(r, lanes_log2, s);
+      default: break;
+    }
+  }
+  if (vpl <= 1) return launch_route_count_t<1, false>(r, lanes_log2, s);
+  if (vpl <= 2) return launch_route_count_t<2, false>(r, lanes_log2, s);
+  if (vpl <= 4) return launch_route_count_t<4, false>(r, lanes_log2, s);
+  if (vpl <= 8) return launch_route_count_t<8, false>(r, lanes_log2, s);
+  if (vpl <= 16) return launch_route_count_t<16, false>(r, lanes_log2, s);
+  return launch_route_count_t<32, false>(r, lanes_log2, s);
 }
 
 }  // namespace ep

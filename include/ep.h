@@ -156,6 +156,23 @@ ep_status_t ep_dispatch(const ep_config_t* cfg, const void* x, const int32_t* to
                         void* ws, size_t ws_bytes, cudaStream_t stream);
 
 /*
+ * ep_route_dispatch — ep_route followed by ep_dispatch in one call, with the
+ * routing fused into the dispatch's per-tile count (ThunderEP on consumer
+ * GPUs, bjdmk.com.cn, §5.2: do the bucketing by destination while routing,
+ * saving a pass). Every output is bit-for-bit what
+ *   ep_route(cfg, logits, topk_idx, topk_w, stream);
+ *   ep_dispatch(cfg, x, topk_idx, payload, ..., ws, ws_bytes, stream);
+ * would write; the arguments mean what they mean there (logits [T, E] fp32
+ * in, 16-byte aligned; topk_idx / topk_w [T, k] out). One kernel fewer runs:
+ * a CTA routes one tile of tokens and counts its per-expert copies in shared
+ * memory, then the scan and the scatter run as in ep_dispatch.
+ */
+ep_status_t ep_route_dispatch(const ep_config_t* cfg, const float* logits, const void* x, int32_t* topk_idx,
+                              float* topk_w, void* payload, float* scales, int32_t* row_slot, int32_t* slot_row,
+                              int32_t* expert_counts, int32_t* expert_raw, int32_t* expert_off, int32_t* rank_off,
+                              int32_t* n_dropped, void* ws, size_t ws_bytes, cudaStream_t stream);
+
+/*
  * ep_dispatch_static — ep_dispatch for callers that cannot allocate device
  * memory. The pages have no counterpart to this call: it exists only for
  * this library's users.

@@ -38,6 +38,24 @@ def _run_path(ep, cfg, logits, x, expert_out):
     return buf
 
 
+_OUTPUTS = ("topk_idx", "topk_w", "slot_row", "expert_counts", "expert_raw", "expert_off", "rank_off", "n_dropped")
+
+
+def _assert_fused_matches(ep, cfg, ref, logits, x):
+    """ep_route_dispatch writes bit-for-bit what ep_route + ep_dispatch wrote."""
+    fused = ep.EpBuffers.allocate(cfg)
+    fused.route_dispatch(logits, x)
+    torch.cuda.synchronize()
+    assert ep.ep_get_error(fused.ws) == ep.EP_OK
+    for name in _OUTPUTS:
+        assert torch.equal(getattr(ref, name), getattr(fused, name)), name
+    N = int(ref.rank_off[-1].item())
+    assert torch.equal(ref.row_slot[:N], fused.row_slot[:N])
+    assert torch.equal(ref.payload[:N].view(torch.uint8), fused.payload[:N].view(torch.uint8))
+    if ref.scales is not None:
+        assert torch.equal(ref.scales[:N], fused.scales[:N])
+
+
 def _check_layout(buf, lay, N):
     np.testing.assert_array_equal(buf.expert_counts.cpu().numpy(), lay["expert_counts"])
     np.testing.assert_array_equal(buf.expert_raw.cpu().numpy(), lay["expert_raw"])
@@ -56,6 +74,7 @@ def _full_parity(ep, orc, w, payload, renormalize=False, device_gen="cuda"):
     d = workloads.generate(w, device=device_gen)
     logits, x, eo = (d[n].cuda() for n in ("logits", "x", "expert_out"))
     buf = _run_path(ep, cfg, logits, x, eo)
+    _assert_fused_matches(ep, cfg, buf, logits, x)
 
     logits_h = logits.cpu().numpy()
     x_bits = _bits(x)
@@ -122,6 +141,7 @@ def test_large_parity_sampled(ep, orc, payload):
     d = workloads.generate(w, device="cuda")
     logits, x, eo = d["logits"], d["x"], d["expert_out"]
     buf = _run_path(ep, cfg, logits, x, eo)
+    _assert_fused_matches(ep, cfg, buf, logits, x)
     idx, wts = orc.route(logits.cpu().numpy(), w.k)
     np.testing.assert_array_equal(buf.topk_idx.cpu().numpy(), idx)
     assert_weights_close(buf.topk_w.cpu().numpy(), wts)
@@ -166,6 +186,8 @@ def test_large_parity_sampled(ep, orc, payload):
 EDGE = [
     # T, H, E, k, R, cf, payload, renorm, note
     (1, 16, 1, 1, 1, 0.0, 0, 0, "one token, one expert, minimum H"),
+    (5, 16, 3, 2, 1, 0.0, 1, 0, "int8 at minimum H: one 16-element group"),
+    (700, 48, 6, 3, 3, 0.0, 1, 0, "int8 with an odd number of 16-element groups"),
     (1000, 64, 8, 2, 2, 0.0, 1, 0, "ragged last tile"),
     (2500, 48, 6, 3, 3, 0.0, 0, 1, "E not a power of two, two ragged tiles"),
     (777, 16384, 4, 2, 2, 0.0, 1, 0, "maximum H"),
@@ -197,6 +219,20 @@ def test_all_ties_pick_lowest_ids(ep, orc):
     torch.cuda.synchronize()
     assert np.all(buf.topk_idx.cpu().numpy() == np.arange(4))
     np.testing.assert_allclose(buf.topk_w.cpu().numpy(), 1.0 / 16, rtol=1e-6)
+
+
+def test_empty_batch_fused(ep):
+    cfg = ep.make_config(0, 64, 8, 2, 2, payload=ep.EP_PAYLOAD_INT8)
+    buf = ep.EpBuffers.allocate(cfg)
+    buf.expert_off.fill_(7)
+    buf.rank_off.fill_(7)
+    buf.n_dropped.fill_(7)
+    buf.route_dispatch(torch.empty(0, 8, device="cuda"), torch.empty(0, 64, dtype=torch.bfloat16, device="cuda"))
+    torch.cuda.synchronize()
+    assert buf.expert_off.cpu().tolist() == [0] * 9
+    assert buf.rank_off.cpu().tolist() == [0] * 3
+    assert buf.n_dropped.item() == 0
+    assert ep.ep_get_error(buf.ws) == ep.EP_OK
 
 
 def test_empty_batch(ep):
