@@ -196,6 +196,7 @@ EDGE = [
     (400, 64, 16, 16, 4, 0.0, 0, 0, "k = E: every expert"),
     (3000, 128, 32, 4, 4, 0.25, 1, 0, "heavy capacity drops"),
     (2048, 256, 64, 6, 8, 1.0, 0, 1, "capacity factor 1.0, bf16"),
+    (40000, 16, 512, 4, 8, 1.0, 1, 0, "many experts x tiles (80,384 tile counts)"),
 ]
 
 
