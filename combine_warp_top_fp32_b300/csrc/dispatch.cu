@@ -13,7 +13,7 @@
 //            tile's tokens in shared memory (atomicOr, order-free); their
 //            popcounts give the tile's per-expert count and each pair's rank
 //            within the tile in token order;
-//   scan     one CTA per expert: the exclusive running sum over tiles (each
+//   scan     one warp per expert: the exclusive running sum over tiles (each
 //            tile's first position within the expert) and the capacity clip;
 //            the last CTA to finish (atomic ticket after a fence — no CTA
 //            ever waits for another) sums the kept counts over experts into
@@ -104,34 +104,62 @@ __device__ __forceinline__ int block_exclusive_scan_256(int v, int& total, int* 
   return wpre + incl - v;
 }
 
-__global__ void __launch_bounds__(256) scan_kernel(const int32_t* __restrict__ tile_counts, int E, int R, int ntiles,
-                                                    int cap, int32_t* __restrict__ tile_base,
-                                                    int32_t* __restrict__ expert_counts,
-                                                    int32_t* __restrict__ expert_raw,
-                                                    int32_t* __restrict__ expert_off, int32_t* __restrict__ rank_off,
-                                                    int32_t* __restrict__ n_dropped, int32_t* kept_g,
-                                                    int32_t* drop_g, uint32_t* ticket) {
+// One warp per expert (eight per CTA): the exclusive running sum of the
+// expert's tile counts (each tile's first position within the expert, eight
+// tiles per lane per pass) and the capacity clip; the last CTA to finish
+// (atomic ticket after a fence — no CTA ever waits for another) sums the kept
+// counts over experts into expert_off / rank_off.
+constexpr int kScanWarps = 8;
+
+__global__ void __launch_bounds__(32 * kScanWarps) scan_kernel(
+    const int32_t* __restrict__ tile_counts, int E, int R, int ntiles, int cap, int32_t* __restrict__ tile_base,
+    int32_t* __restrict__ expert_counts, int32_t* __restrict__ expert_raw, int32_t* __restrict__ expert_off,
+    int32_t* __restrict__ rank_off, int32_t* __restrict__ n_dropped, int32_t* kept_g, int32_t* drop_g,
+    uint32_t* ticket) {
+  constexpr int V = 8;
   __shared__ int warp_s[8];
   __shared__ int is_last;
-  const int e = blockIdx.x;
-  pdl_wait();  // tile counts come from the count kernel
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int e = blockIdx.x * kScanWarps + warp;
+  pdl_wait();  // tile counts come from the counting kernel
   pdl_launch_dependents();
-  // this expert's running sum over tiles
-  int carry = 0;
-  for (int c0 = 0; c0 < ntiles; c0 += blockDim.x) {
-    const int i = c0 + threadIdx.x;
-    const int v = i < ntiles ? tile_counts[static_cast<int64_t>(e) * ntiles + i] : 0;
-    int tot;
-    const int ex = block_exclusive_scan_256(v, tot, warp_s);
-    if (i < ntiles) tile_base[static_cast<int64_t>(e) * ntiles + i] = carry + ex;
-    carry += tot;
+  if (e < E) {
+    const int32_t* tc = tile_counts + static_cast<int64_t>(e) * ntiles;
+    int32_t* tb = tile_base + static_cast<int64_t>(e) * ntiles;
+    int carry = 0;
+    for (int c0 = 0; c0 < ntiles; c0 += 32 * V) {
+      int v[V];
+#pragma unroll
+      for (int j = 0; j < V; ++j) {
+        const int i = c0 + lane * V + j;
+        v[j] = i < ntiles ? tc[i] : 0;
+      }
+      int run = 0;
+#pragma unroll
+      for (int j = 0; j < V; ++j) {
+        const int x = v[j];
+        v[j] = run;
+        run += x;
+      }
+      const int incl = warp_inclusive_scan(run);
+      const int base = carry + incl - run;
+#pragma unroll
+      for (int j = 0; j < V; ++j) {
+        const int i = c0 + lane * V + j;
+        if (i < ntiles) tb[i] = base + v[j];
+      }
+      carry += __shfl_sync(0xffffffffu, incl, 31);
+    }
+    if (lane == 0) {
+      const int kept = min(carry, cap);
+      expert_counts[e] = kept;
+      if (expert_raw) expert_raw[e] = carry;
+      kept_g[e] = kept;
+      drop_g[e] = carry - kept;
+    }
   }
+  __syncthreads();
   if (threadIdx.x == 0) {
-    const int kept = min(carry, cap);
-    expert_counts[e] = kept;
-    if (expert_raw) expert_raw[e] = carry;
-    kept_g[e] = kept;
-    drop_g[e] = carry - kept;
     __threadfence();
     const unsigned prev = atomicAdd(ticket, 1u);
     is_last = (prev == static_cast<unsigned>(gridDim.x) - 1u);
@@ -142,6 +170,7 @@ __global__ void __launch_bounds__(256) scan_kernel(const int32_t* __restrict__ t
   // last CTA: every other CTA's kept/drop values are visible (fence + ticket)
   __threadfence();
   int carry_off = 0, drops = 0;
+  const int G = E / R;  // rank r starts at its first expert r*G
   for (int c0 = 0; c0 < E; c0 += blockDim.x) {
     const int i = c0 + threadIdx.x;
     const int v = i < E ? __ldcg(kept_g + i) : 0;
@@ -150,8 +179,6 @@ __global__ void __launch_bounds__(256) scan_kernel(const int32_t* __restrict__ t
     const int ex = block_exclusive_scan_256(v, tot, warp_s);
     block_exclusive_scan_256(d, dtot, warp_s);
     if (i < E) expert_off[i] = carry_off + ex;
-    // rank r starts at its first expert r*G
-    const int G = E / R;
     if (i < E && i % G == 0) rank_off[i / G] = carry_off + ex;
     carry_off += tot;
     drops += dtot;
@@ -432,8 +459,9 @@ cudaError_t launch_dispatch(const DispatchArgs& a, int sms, cudaStream_t s) {
 }
 
 cudaError_t launch_scan_scatter(const DispatchArgs& a, int sms, cudaStream_t s) {
-  cudaError_t err = launch_pdl(scan_kernel, a.E, 256, 0, s, a.tile_counts, a.E, a.R, a.ntiles, a.cap, a.tile_base, a.expert_counts,
-                   a.expert_raw, a.expert_off, a.rank_off, a.n_dropped, a.kept, a.dropped, a.ticket);
+  cudaError_t err = launch_pdl(scan_kernel, (a.E + kScanWarps - 1) / kScanWarps, 32 * kScanWarps, 0, s,
+                               a.tile_counts, a.E, a.R, a.ntiles, a.cap, a.tile_base, a.expert_counts, a.expert_raw,
+                               a.expert_off, a.rank_off, a.n_dropped, a.kept, a.dropped, a.ticket);
   if (err != cudaSuccess) return err;
   if (a.T == 0) return cudaSuccess;
 

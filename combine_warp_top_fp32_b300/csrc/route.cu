@@ -27,11 +27,12 @@ namespace ep {
 namespace {
 
 // Float -> unsigned key whose unsigned order is the float order; -0 and +0
-// map to the same key (they compare equal as floats).
+// map to the same key (they compare equal as floats): adding +0 turns -0 into
+// +0 and leaves every other value unchanged; then negative values have all
+// bits flipped and non-negative ones only the sign bit.
 __device__ __forceinline__ uint32_t ordered_bits(float v) {
-  uint32_t u = __float_as_uint(v);
-  if ((u & 0x7fffffffu) == 0u) u = 0u;  // -0 -> +0
-  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+  const uint32_t u = __float_as_uint(__fadd_rn(v, 0.0f));
+  return u ^ (static_cast<uint32_t>(static_cast<int32_t>(u) >> 31) | 0x80000000u);
 }
 
 __device__ __forceinline__ float key_value(uint64_t key) {
@@ -275,6 +276,117 @@ __device__ __forceinline__ void route_token(const float* __restrict__ logits, in
   *w_out = __fdiv_rn(exp_shifted(my_v, l_max), denom);
 }
 
+// NQ tokens per warp at once (one token per 32 lanes, E >= 32, at most 8
+// values per lane; the kernels use NQ = 2 up to 4 values per lane, where the
+// doubled registers still leave room for many warps): the same steps as route_token on the sorted-key path, with
+// every per-token value held for all NQ tokens so that the NQ independent
+// chains of reductions and exponentials interleave in one warp. On return lane
+// j < k holds slot j of token q in e_out[q] / w_out[q].
+template <int NQ, int VPL, bool VEC4>
+__device__ __forceinline__ void route_tokens_sorted(const float* __restrict__ logits, const int64_t (&t)[NQ],
+                                                    const bool (&active)[NQ], int E, int k, int lane, int renorm,
+                                                    int (&e_out)[NQ], float (&w_out)[NQ]) {
+  float val[NQ][VPL];
+  uint64_t key[NQ][VPL];
+#pragma unroll
+  for (int q = 0; q < NQ; ++q) {
+    const float* row = logits + (active[q] ? t[q] : 0) * static_cast<int64_t>(E);
+    if constexpr (VEC4) {
+#pragma unroll
+      for (int i = 0; i < VPL / 4; ++i) {
+        const int e0 = 4 * lane + 128 * i;
+        float4 f = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (active[q]) f = __ldg(reinterpret_cast<const float4*>(row + e0));
+        val[q][4 * i + 0] = f.x;
+        val[q][4 * i + 1] = f.y;
+        val[q][4 * i + 2] = f.z;
+        val[q][4 * i + 3] = f.w;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) key[q][4 * i + c] = active[q] ? make_key(val[q][4 * i + c], e0 + c) : 0ull;
+      }
+    } else {
+#pragma unroll
+      for (int i = 0; i < VPL; ++i) {
+        const int e = lane + 32 * i;
+        const bool ok = active[q] && e < E;
+        val[q][i] = ok ? __ldg(row + e) : 0.f;
+        key[q][i] = ok ? make_key(val[q][i], e) : 0ull;
+      }
+    }
+  }
+#pragma unroll
+  for (int q = 0; q < NQ; ++q) sort_desc<VPL>(key[q]);
+
+  uint32_t my_bits[NQ], max_bits[NQ];
+#pragma unroll
+  for (int q = 0; q < NQ; ++q) {
+    my_bits[q] = 0u;
+    max_bits[q] = 0u;
+    e_out[q] = 0;
+  }
+  for (int r = 0; r < k; ++r) {
+    uint32_t gmax[NQ], cand[NQ], win[NQ];
+#pragma unroll
+    for (int q = 0; q < NQ; ++q) gmax[q] = __reduce_max_sync(0xffffffffu, static_cast<uint32_t>(key[q][0] >> 32));
+#pragma unroll
+    for (int q = 0; q < NQ; ++q)
+      cand[q] = (static_cast<uint32_t>(key[q][0] >> 32) == gmax[q]) ? 0xffffffffu - static_cast<uint32_t>(key[q][0])
+                                                                      : 0xffffffffu;
+#pragma unroll
+    for (int q = 0; q < NQ; ++q) win[q] = __reduce_min_sync(0xffffffffu, cand[q]);
+#pragma unroll
+    for (int q = 0; q < NQ; ++q) {
+      if (r == 0) max_bits[q] = gmax[q];
+      if (lane == r) {
+        e_out[q] = static_cast<int>(win[q]);
+        my_bits[q] = gmax[q];
+      }
+      if (cand[q] == win[q]) {
+#pragma unroll
+        for (int i = 0; i + 1 < VPL; ++i) key[q][i] = key[q][i + 1];
+        key[q][VPL - 1] = 0ull;  // 0 is below every real key
+      }
+    }
+  }
+
+  float l_max[NQ], my_v[NQ], s[NQ], c[NQ];
+#pragma unroll
+  for (int q = 0; q < NQ; ++q) {
+    l_max[q] = key_value(static_cast<uint64_t>(max_bits[q]) << 32);
+    my_v[q] = key_value(static_cast<uint64_t>(my_bits[q]) << 32);
+    s[q] = 0.f;
+    c[q] = 0.f;
+  }
+  if (renorm) {
+#pragma unroll
+    for (int q = 0; q < NQ; ++q)
+      if (lane < k) s[q] = exp_shifted_term(my_v[q], l_max[q]);
+  } else {
+#pragma unroll
+    for (int i = 0; i < VPL; ++i)
+#pragma unroll
+      for (int q = 0; q < NQ; ++q) {
+        const bool ok = VEC4 ? active[q] : (active[q] && (lane + 32 * i) < E);
+        if (ok) comp_add(s[q], c[q], exp_shifted_term(val[q][i], l_max[q]));
+      }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+#pragma unroll
+    for (int q = 0; q < NQ; ++q) {
+      const float s2 = __shfl_xor_sync(0xffffffffu, s[q], o);
+      const float c2 = __shfl_xor_sync(0xffffffffu, c[q], o);
+      const float tt = __fadd_rn(s[q], s2);
+      const float bb = __fsub_rn(tt, s[q]);
+      const float err = __fadd_rn(__fsub_rn(s[q], __fsub_rn(tt, bb)), __fsub_rn(s2, bb));
+      c[q] = __fadd_rn(__fadd_rn(c[q], c2), err);
+      s[q] = tt;
+    }
+  }
+#pragma unroll
+  for (int q = 0; q < NQ; ++q) w_out[q] = __fdiv_rn(exp_shifted(my_v[q], l_max[q]), __fadd_rn(s[q], c[q]));
+}
+
 template <int VPL, bool VEC4>
 __global__ void __launch_bounds__(256) route_topk_kernel(const float* __restrict__ logits, int T, int E, int k,
                                                          int lanes_log2, int renorm, int32_t* __restrict__ topk_idx,
@@ -289,6 +401,24 @@ __global__ void __launch_bounds__(256) route_topk_kernel(const float* __restrict
   pdl_wait();  // the logits may come from the kernel before this one
   pdl_launch_dependents();
 
+  if constexpr (VPL <= 4) {
+    if (L == 32) {  // two tokens per warp in flight: tokens w and w + n_warps
+      for (int64_t tb = warp_id; tb < T; tb += 2 * n_warps) {
+        const int64_t tq[2] = {tb, tb + n_warps};
+        const bool act[2] = {true, tb + n_warps < T};
+        int e[2];
+        float w[2];
+        route_tokens_sorted<2, VPL, VEC4>(logits, tq, act, E, k, lane, renorm, e, w);
+#pragma unroll
+        for (int q = 0; q < 2; ++q)
+          if (act[q] && lane < k) {
+            topk_idx[tq[q] * k + lane] = e[q];
+            topk_w[tq[q] * k + lane] = w[q];
+          }
+      }
+      return;
+    }
+  }
   for (int64_t tb = warp_id * groups_per_warp; tb < T; tb += n_warps * groups_per_warp) {
     const int64_t t = tb + grp;
     const bool active = t < T;
@@ -333,17 +463,40 @@ __global__ void __launch_bounds__(VPL >= 16 ? 256 : 512) route_count_kernel(
   __syncthreads();
   if (nt <= 0) return;  // an empty batch: only the ticket
 
-  for (int tl0 = warp * groups_per_warp; tl0 < nt; tl0 += nw * groups_per_warp) {
-    const int tl = tl0 + grp;
-    const bool active = tl < nt;
-    const int64_t t = t0 + tl;
-    int e;
-    float w;
-    route_token<VPL, VEC4>(logits, t, active, E, k, L, sub, renorm, &e, &w);
-    if (active && sub < k) {
-      topk_idx[t * k + sub] = e;
-      topk_w[t * k + sub] = w;
-      atomicOr(&mask[e * TW + (tl >> 5)], 1u << (tl & 31));
+  bool routed = false;
+  if constexpr (VPL <= 4) {
+    if (L == 32) {  // two tokens per warp in flight: tile tokens w and w + nw
+      for (int tl0 = warp; tl0 < nt; tl0 += 2 * nw) {
+        const int tlq[2] = {tl0, tl0 + nw};
+        const int64_t tq[2] = {t0 + tl0, t0 + tl0 + nw};
+        const bool act[2] = {true, tl0 + nw < nt};
+        int e[2];
+        float w[2];
+        route_tokens_sorted<2, VPL, VEC4>(logits, tq, act, E, k, lane, renorm, e, w);
+#pragma unroll
+        for (int q = 0; q < 2; ++q)
+          if (act[q] && lane < k) {
+            topk_idx[tq[q] * k + lane] = e[q];
+            topk_w[tq[q] * k + lane] = w[q];
+            atomicOr(&mask[e[q] * TW + (tlq[q] >> 5)], 1u << (tlq[q] & 31));
+          }
+      }
+      routed = true;
+    }
+  }
+  if (!routed) {
+    for (int tl0 = warp * groups_per_warp; tl0 < nt; tl0 += nw * groups_per_warp) {
+      const int tl = tl0 + grp;
+      const bool active = tl < nt;
+      const int64_t t = t0 + tl;
+      int e;
+      float w;
+      route_token<VPL, VEC4>(logits, t, active, E, k, L, sub, renorm, &e, &w);
+      if (active && sub < k) {
+        topk_idx[t * k + sub] = e;
+        topk_w[t * k + sub] = w;
+        atomicOr(&mask[e * TW + (tl >> 5)], 1u << (tl & 31));
+      }
     }
   }
   __syncthreads();

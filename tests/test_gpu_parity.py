@@ -251,11 +251,15 @@ def test_empty_batch(ep):
     assert ep.ep_get_error(buf.ws) == ep.EP_OK
 
 
-def test_int8_return_path(ep, orc):
-    """Expert outputs coded per row (ep_quantize_rows) then combined as int8."""
+@pytest.mark.parametrize("shape", ["prefill-mid", "wide"])
+def test_int8_return_path(ep, orc, shape):
+    """Expert outputs coded per row (ep_quantize_rows) then combined as int8
+    (prefill-mid: 2 KB int8 rows; wide: 8 KB int8 rows, with drops)."""
     from combine_warp_top_fp32_b300 import workloads
 
     w = workloads.WORKLOADS["prefill-mid"]
+    if shape == "wide":
+        w = w.replace(T=1500, H=8192, capacity_factor=1.0, seed=9)
     cfg = ep.config_from_workload(w, payload=ep.EP_PAYLOAD_INT8)
     d = workloads.generate(w, device="cuda")
     rows = w.max_rows()
