@@ -14,7 +14,9 @@ Functions and the passages they follow:
 * :func:`layout` — per-expert counts, capacity cap, offsets as running sums and
   the rank-major row order (NCCL EP article, hotelren.com, §3.3 flat sendbuff;
   ThunderEP on consumer GPUs, bjdmk.com.cn, §2.1 aggregation).
-* :func:`quantize_rows` / :func:`payload` — per-token int8 code (ThunderEP §2.3).
+* :func:`quantize_rows` / :func:`payload` — per-token int8 code (ThunderEP §2.3),
+  or the same per-token scheme with an FP8 E4M3 code (ThunderEP §5.2; NCCL EP
+  article §6.3).
 * :func:`combine` — gate-weighted sum of the k expert outputs (ThunderEP §1.3).
 """
 from __future__ import annotations
@@ -68,6 +70,14 @@ def _bind(lib):
     lib.oracle_payload.argtypes = [I, I, I, I, I, P, P, P, P]
     lib.oracle_dequant.argtypes = [ctypes.c_int8, ctypes.c_float]
     lib.oracle_dequant.restype = ctypes.c_float
+    lib.oracle_dequant_fp8.argtypes = [ctypes.c_uint8, ctypes.c_float]
+    lib.oracle_dequant_fp8.restype = ctypes.c_float
+    lib.oracle_quantize_row_fp8.argtypes = [I, P, P, P]
+    lib.oracle_quantize_rows_fp8.argtypes = [I, I, P, P, P]
+    lib.oracle_float_to_e4m3.argtypes = [ctypes.c_float]
+    lib.oracle_float_to_e4m3.restype = ctypes.c_uint8
+    lib.oracle_e4m3_to_float.argtypes = [ctypes.c_uint8]
+    lib.oracle_e4m3_to_float.restype = ctypes.c_float
     lib.oracle_combine.argtypes = [I, I, I, I, P, P, P, P, P]
     lib.oracle_combine_tokens.argtypes = [I, P, I, I, I, P, P, P, P, P]
     lib.oracle_count_cv.argtypes = [I, P]
@@ -89,6 +99,14 @@ def _p(a: np.ndarray | None):
 def _check(rc: int, what: str):
     if rc != 0:
         raise ValueError(f"oracle {what} rejected its arguments (rc={rc})")
+
+
+def _out_mode(expert_out: np.ndarray) -> int:
+    """Expert-output format from the array's dtype: uint16 bf16 bits, int8 codes, uint8 E4M3 codes."""
+    modes = {np.dtype(np.uint16): 0, np.dtype(np.int8): 1, np.dtype(np.uint8): 2}
+    if expert_out.dtype not in modes:
+        raise ValueError(f"unsupported expert output dtype {expert_out.dtype}")
+    return modes[expert_out.dtype]
 
 
 class Oracle:
@@ -134,45 +152,61 @@ class Oracle:
                     slot_row=slot_row, row_slot=row_slot[:N].copy(), n_dropped=int(nd[0]), N=N)
 
     # step 5
-    def quantize_rows(self, x_bits: np.ndarray):
+    def quantize_rows(self, x_bits: np.ndarray, fp8: bool = False):
+        """Per-row int8 codes (int8 array), or E4M3 codes (uint8 array) with fp8=True."""
         x_bits = np.ascontiguousarray(x_bits, dtype=np.uint16)
         n, H = x_bits.shape
-        q = np.empty((n, H), np.int8)
         s = np.empty(n, np.float32)
-        _check(self.lib.oracle_quantize_rows(n, H, _p(x_bits), _p(q), _p(s)), "quantize_rows")
+        if fp8:
+            q = np.empty((n, H), np.uint8)
+            _check(self.lib.oracle_quantize_rows_fp8(n, H, _p(x_bits), _p(q), _p(s)), "quantize_rows_fp8")
+        else:
+            q = np.empty((n, H), np.int8)
+            _check(self.lib.oracle_quantize_rows(n, H, _p(x_bits), _p(q), _p(s)), "quantize_rows")
         return q, s
 
-    def payload(self, x_bits: np.ndarray, row_slot: np.ndarray, k: int, int8: bool):
+    def payload(self, x_bits: np.ndarray, row_slot: np.ndarray, k: int, mode):
+        """mode: 0/False bf16 bytes, 1/True int8 code, 2 FP8 E4M3 code (uint8)."""
+        mode = int(mode)
         x_bits = np.ascontiguousarray(x_bits, dtype=np.uint16)
         row_slot = np.ascontiguousarray(row_slot, dtype=np.int32)
         T, H = x_bits.shape
         N = row_slot.shape[0]
-        if int8:
+        if mode == 1:
             pl = np.empty((N, H), np.int8)
+            sc = np.empty(N, np.float32)
+        elif mode == 2:
+            pl = np.empty((N, H), np.uint8)
             sc = np.empty(N, np.float32)
         else:
             pl = np.empty((N, H), np.uint16)
             sc = None
-        _check(self.lib.oracle_payload(T, H, k, N, int(bool(int8)), _p(x_bits), _p(row_slot), _p(pl),
-                                       _p(sc)), "payload")
+        _check(self.lib.oracle_payload(T, H, k, N, mode, _p(x_bits), _p(row_slot), _p(pl), _p(sc)), "payload")
         return pl, sc
 
     def dequant(self, q: int, scale: float) -> float:
         return float(self.lib.oracle_dequant(int(q), float(scale)))
+
+    def dequant_fp8(self, code: int, scale: float) -> float:
+        return float(self.lib.oracle_dequant_fp8(int(code), float(scale)))
+
+    def float_to_e4m3(self, v: float) -> int:
+        return int(self.lib.oracle_float_to_e4m3(float(v)))
+
+    def e4m3_to_float(self, code: int) -> float:
+        return float(self.lib.oracle_e4m3_to_float(int(code)))
 
     # step 7
     def combine(self, expert_out: np.ndarray, out_scales: np.ndarray | None, slot_row: np.ndarray,
                 topk_w: np.ndarray, T: int, k: int):
         expert_out = np.ascontiguousarray(expert_out)
         H = expert_out.shape[1]
-        out_int8 = expert_out.dtype == np.int8
-        if not out_int8:
-            assert expert_out.dtype == np.uint16
+        out_mode = _out_mode(expert_out)
         slot_row = np.ascontiguousarray(slot_row, dtype=np.int32).reshape(-1)
         topk_w = np.ascontiguousarray(topk_w, dtype=np.float32).reshape(-1)
         sc = None if out_scales is None else np.ascontiguousarray(out_scales, dtype=np.float32)
         y = np.empty((T, H), np.uint16)
-        _check(self.lib.oracle_combine(T, H, k, int(out_int8), _p(expert_out), _p(sc), _p(slot_row),
+        _check(self.lib.oracle_combine(T, H, k, out_mode, _p(expert_out), _p(sc), _p(slot_row),
                                        _p(topk_w), _p(y)), "combine")
         return y
 
@@ -180,12 +214,12 @@ class Oracle:
         tokens = np.ascontiguousarray(tokens, dtype=np.int32)
         expert_out = np.ascontiguousarray(expert_out)
         H = expert_out.shape[1]
-        out_int8 = expert_out.dtype == np.int8
+        out_mode = _out_mode(expert_out)
         slot_row = np.ascontiguousarray(slot_row, dtype=np.int32).reshape(-1)
         topk_w = np.ascontiguousarray(topk_w, dtype=np.float32).reshape(-1)
         sc = None if out_scales is None else np.ascontiguousarray(out_scales, dtype=np.float32)
         y = np.empty((tokens.shape[0], H), np.uint16)
-        _check(self.lib.oracle_combine_tokens(tokens.shape[0], _p(tokens), H, k, int(out_int8), _p(expert_out),
+        _check(self.lib.oracle_combine_tokens(tokens.shape[0], _p(tokens), H, k, out_mode, _p(expert_out),
                                               _p(sc), _p(slot_row), _p(topk_w), _p(y)), "combine_tokens")
         return y
 
@@ -205,7 +239,7 @@ class Oracle:
         T, E = logits.shape
         idx, w = self.route(logits, k, renormalize)
         lay = self.layout(idx, E, R, capacity_factor)
-        pl, sc = self.payload(x_bits, lay["row_slot"], k, payload_int8)
+        pl, sc = self.payload(x_bits, lay["row_slot"], k, int(payload_int8))
         y = self.combine(expert_out, out_scales, lay["slot_row"], w, T, k)
         return dict(topk_idx=idx, topk_w=w, payload=pl, scales=sc, y=y, **lay)
 

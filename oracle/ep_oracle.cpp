@@ -21,7 +21,9 @@
 //                 (ThunderEP on consumer GPUs, bjdmk.com.cn, §2.1 "aggregate
 //                  by target card"; NCCL EP article §3.3)
 //   5. payload    per-token dynamic int8 quantisation, one scale per token
-//                 (ThunderEP §2.3 "per-token dynamic quantisation")
+//                 (ThunderEP §2.3 "per-token dynamic quantisation"); or the
+//                 same per-token scheme with an FP8 E4M3 code (ThunderEP §5.2
+//                 "lower-precision payloads"; NCCL EP article §6.3 FP8)
 //   6. dequant    v = q * scale at the receiver (ThunderEP §2.3)
 //   7. combine    gate-weighted sum of the k expert outputs back at the source
 //                 (ThunderEP §1.3, steps 3 and 4 of the EP flow; §3.3 combine)
@@ -62,6 +64,46 @@ uint16_t float_to_bf16_bits_rne(float f) {
   uint32_t upper = u >> 16;
   if (lower > 0x8000u || (lower == 0x8000u && (upper & 1u))) upper += 1u;
   return static_cast<uint16_t>(upper);
+}
+
+// ---- FP8 E4M3, written out from the format: sign bit, 4 exponent bits with
+// bias 7, 3 mantissa bits; exponent field 0 holds subnormals m * 2^-9; no
+// infinities; the all-ones pattern S.1111.111 is NaN, so the largest finite
+// magnitude is 1.75 * 2^8 = 448 (code 0x7e). -----------------------------------
+
+double e4m3_magnitude(int code7) {  // code without its sign bit, not NaN
+  const int ex = (code7 >> 3) & 15, m = code7 & 7;
+  if (ex == 0) return std::ldexp(static_cast<double>(m), -9);
+  return std::ldexp(1.0 + m / 8.0, ex - 7);
+}
+
+float e4m3_code_to_float(uint8_t c) {
+  const double v = e4m3_magnitude(c & 0x7f);
+  return static_cast<float>((c & 0x80) ? -v : v);
+}
+
+// Nearest E4M3 value of a finite float, ties to the even code (the one whose
+// last mantissa bit is 0), magnitudes above 448 saturated to 448; the sign of
+// zero is kept. In each binade [2^e, 2^(e+1)) the representable values are
+// spaced 2^(e-3) (2^-9 below 2^-6), so |v| / spacing is exact in double and
+// rounding it to the nearest integer, ties to even, is the nearest value.
+uint8_t float_to_e4m3_rne_sat(float v) {
+  const uint8_t sign = std::signbit(v) ? 0x80 : 0x00;
+  double a = std::fabs(static_cast<double>(v));
+  if (a > 448.0) a = 448.0;
+  if (a == 0.0) return sign;
+  int e2;
+  std::frexp(a, &e2);        // a = f * 2^e2 with f in [0.5, 1)
+  int ex = e2 - 1;           // a in [2^ex, 2^(ex+1))
+  if (ex < -6) ex = -6;      // the subnormal spacing
+  const double spacing = std::ldexp(1.0, ex - 3);
+  const double r = std::nearbyint(a / spacing);  // default rounding: nearest, ties to even
+  const double val = r * spacing;                // exactly representable (maybe the next binade)
+  if (val < std::ldexp(1.0, -6)) return static_cast<uint8_t>(sign | static_cast<int>(r));  // subnormal m
+  std::frexp(val, &e2);
+  const int vex = e2 - 1;
+  const int m = static_cast<int>((std::ldexp(val, -vex) - 1.0) * 8.0);
+  return static_cast<uint8_t>(sign | ((vex + 7) << 3) | m);
 }
 
 // "a ranks before b" for expert selection: larger logit first, and on equal
@@ -237,22 +279,63 @@ int oracle_quantize_rows(int n, int H, const uint16_t* in, int8_t* q, float* sca
 }
 
 // ---------------------------------------------------------------------------
+// Step 5, FP8 variant — the same per-token scheme with an E4M3 code (ThunderEP
+// §5.2 lists FP8 among the lower-precision payloads; the NCCL EP article, §6.3,
+// uses FP8 for the exchanged data while routing scores stay in high precision).
+//   a     = max_h |x_h|
+//   scale = a / 448.0f                (448 = largest E4M3 magnitude; fp32 IEEE)
+//   q_h   = E4M3 nearest-even of fl(x_h / scale), saturated to +-448
+// Reading (pages silent): the scale maps the row's largest magnitude to the
+// largest finite code, as the int8 code maps it to 127; a == 0 codes every
+// element as +0 with scale 0.
+// ---------------------------------------------------------------------------
+int oracle_quantize_row_fp8(int H, const uint16_t* x_row, uint8_t* q_row, float* scale_out) {
+  if (H < 0) return -1;
+  float a = 0.0f;
+  for (int h = 0; h < H; ++h) {
+    const float v = std::fabs(bf16_bits_to_float(x_row[h]));
+    if (v > a) a = v;
+  }
+  const float scale = a / 448.0f;
+  for (int h = 0; h < H; ++h)
+    q_row[h] = scale == 0.0f ? 0 : float_to_e4m3_rne_sat(bf16_bits_to_float(x_row[h]) / scale);
+  *scale_out = scale;
+  return 0;
+}
+
+int oracle_quantize_rows_fp8(int n, int H, const uint16_t* in, uint8_t* q, float* scales) {
+  if (n < 0 || H < 0) return -1;
+  for (int i = 0; i < n; ++i)
+    oracle_quantize_row_fp8(H, in + static_cast<size_t>(i) * H, q + static_cast<size_t>(i) * H, &scales[i]);
+  return 0;
+}
+
+// E4M3 helpers exported for the tests' pins of the oracle's conversions.
+uint8_t oracle_float_to_e4m3(float v) { return float_to_e4m3_rne_sat(v); }
+float oracle_e4m3_to_float(uint8_t c) { return e4m3_code_to_float(c); }
+
+// ---------------------------------------------------------------------------
 // Step 4+5 — the dispatch payload (ThunderEP §2.1 "aggregate by target card"
 // then §2.3 compression): every kept row is a copy of its token's x row,
-// bf16 bytes unchanged (payload_int8 = 0), or that token's int8 code and
-// scale (payload_int8 = 1). Rows are written from row_slot, N rows.
-// payload is [N, H] uint16 (bf16) or int8; scales is [N] (int8 mode only).
+// bf16 bytes unchanged (mode 0), that token's int8 code and scale (mode 1),
+// or its FP8 E4M3 code and scale (mode 2). Rows are written from row_slot,
+// N rows. payload is [N, H] uint16 (bf16), int8 or uint8 (E4M3 codes);
+// scales is [N] (modes 1 and 2).
 // ---------------------------------------------------------------------------
-int oracle_payload(int T, int H, int k, int N, int payload_int8, const uint16_t* x,
+int oracle_payload(int T, int H, int k, int N, int mode, const uint16_t* x,
                    const int32_t* row_slot, void* payload, float* scales) {
-  if (T < 0 || H < 0 || k < 1 || N < 0) return -1;
+  if (T < 0 || H < 0 || k < 1 || N < 0 || mode < 0 || mode > 2) return -1;
   std::vector<int8_t> q(static_cast<size_t>(H));
   for (int row = 0; row < N; ++row) {
     const int32_t s = row_slot[row];
     if (s < 0 || s >= T * k) return -2;
     const int t = s / k;
     const uint16_t* xr = x + static_cast<size_t>(t) * H;
-    if (payload_int8) {
+    if (mode == 2) {
+      float scale;
+      oracle_quantize_row_fp8(H, xr, static_cast<uint8_t*>(payload) + static_cast<size_t>(row) * H, &scale);
+      scales[row] = scale;
+    } else if (mode == 1) {
       float scale;
       oracle_quantize_row(H, xr, q.data(), &scale);
       std::memcpy(static_cast<int8_t*>(payload) + static_cast<size_t>(row) * H, q.data(),
@@ -269,6 +352,7 @@ int oracle_payload(int T, int H, int k, int N, int payload_int8, const uint16_t*
 // Step 6 — dequantised value of one element: one fp32 multiply (ThunderEP §2.3,
 // "decompress back at the target card").
 float oracle_dequant(int8_t q, float scale) { return static_cast<float>(q) * scale; }
+float oracle_dequant_fp8(uint8_t q, float scale) { return e4m3_code_to_float(q) * scale; }
 
 // ---------------------------------------------------------------------------
 // Step 7 — combine (ThunderEP §1.3: the expert's card sends results back and
@@ -279,12 +363,13 @@ float oracle_dequant(int8_t q, float scale) { return static_cast<float>(q) * sca
 //   y[t,h] = bf16 round-to-nearest-even of acc.
 // Reading: fused multiply-add per slot (the pages fix no order or rounding;
 // fixed slot order is what makes the result reproducible).
-// out_int8 = 0: expert_out is [*, H] bf16 bits; 1: int8 with out_scales[*].
+// out_mode 0: expert_out is [*, H] bf16 bits; 1: int8 codes with
+// out_scales[*]; 2: E4M3 codes with out_scales[*].
 // ---------------------------------------------------------------------------
-int oracle_combine(int T, int H, int k, int out_int8, const void* expert_out,
+int oracle_combine(int T, int H, int k, int out_mode, const void* expert_out,
                    const float* out_scales, const int32_t* slot_row, const float* topk_w,
                    uint16_t* y) {
-  if (T < 0 || H < 0 || k < 1) return -1;
+  if (T < 0 || H < 0 || k < 1 || out_mode < 0 || out_mode > 2) return -1;
   for (int t = 0; t < T; ++t) {
     for (int h = 0; h < H; ++h) {
       float acc = 0.0f;
@@ -293,7 +378,9 @@ int oracle_combine(int T, int H, int k, int out_int8, const void* expert_out,
         if (row < 0) continue;
         const size_t at = static_cast<size_t>(row) * H + h;
         float v;
-        if (out_int8)
+        if (out_mode == 2)
+          v = oracle_dequant_fp8(static_cast<const uint8_t*>(expert_out)[at], out_scales[row]);
+        else if (out_mode == 1)
           v = oracle_dequant(static_cast<const int8_t*>(expert_out)[at], out_scales[row]);
         else
           v = bf16_bits_to_float(static_cast<const uint16_t*>(expert_out)[at]);
@@ -307,7 +394,7 @@ int oracle_combine(int T, int H, int k, int out_int8, const void* expert_out,
 
 // Combine for a subset of tokens only (sampled parity at full size): y rows
 // are written in the order of `tokens`.
-int oracle_combine_tokens(int n_tokens, const int32_t* tokens, int H, int k, int out_int8,
+int oracle_combine_tokens(int n_tokens, const int32_t* tokens, int H, int k, int out_mode,
                           const void* expert_out, const float* out_scales,
                           const int32_t* slot_row, const float* topk_w, uint16_t* y) {
   for (int i = 0; i < n_tokens; ++i) {
@@ -320,7 +407,9 @@ int oracle_combine_tokens(int n_tokens, const int32_t* tokens, int H, int k, int
         if (row < 0) continue;
         const size_t at = static_cast<size_t>(row) * H + h;
         float v;
-        if (out_int8)
+        if (out_mode == 2)
+          v = oracle_dequant_fp8(static_cast<const uint8_t*>(expert_out)[at], out_scales[row]);
+        else if (out_mode == 1)
           v = oracle_dequant(static_cast<const int8_t*>(expert_out)[at], out_scales[row]);
         else
           v = bf16_bits_to_float(static_cast<const uint16_t*>(expert_out)[at]);

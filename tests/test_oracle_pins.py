@@ -434,3 +434,114 @@ def test_count_cv_closed_forms(orc):
     assert orc.count_cv(np.array([5, 5, 5, 5], np.int32)) == 0.0
     assert orc.count_cv(np.array([0, 2], np.int32)) == 1.0
     assert abs(orc.count_cv(np.array([1, 2, 3], np.int32)) - math.sqrt(2 / 3) / 2) < 1e-15
+
+
+# ----------------------------------------------------------------------------
+# FP8 E4M3 per-token payload (ThunderEP §5.2 lower-precision payloads; NCCL EP
+# article §6.3 FP8 for the exchanged data): the oracle's E4M3 conversions
+# against torch's float8_e4m3fn and against brute force over all 256 codes.
+# ----------------------------------------------------------------------------
+_E4M3_NAN = (0x7F, 0xFF)
+
+
+def _e4m3_table():
+    codes = np.array([c for c in range(256) if c not in _E4M3_NAN], dtype=np.uint8)
+    vals = torch.from_numpy(codes).view(torch.float8_e4m3fn).float().numpy().astype(np.float64)
+    return codes, vals
+
+
+def test_e4m3_decode_matches_torch(orc):
+    codes, vals = _e4m3_table()
+    got = np.array([orc.e4m3_to_float(int(c)) for c in codes], dtype=np.float64)
+    np.testing.assert_array_equal(got, vals)
+    assert orc.e4m3_to_float(0x7E) == 448.0 and orc.e4m3_to_float(0x01) == 2.0 ** -9
+
+
+def _brute_force_e4m3(v: float) -> int:
+    """Nearest E4M3 code by scanning every code (ties: the code with an even
+    last mantissa bit), magnitudes above 448 saturated."""
+    codes, vals = _e4m3_table()
+    a = min(abs(v), 448.0)
+    pos = codes < 0x80
+    c, x = codes[pos], vals[pos]
+    d = np.abs(x - a)
+    best = np.flatnonzero(d == d.min())
+    if best.size > 1:
+        best = best[(c[best] & 1) == 0]
+    code = int(c[best[0]])
+    return code | (0x80 if math.copysign(1.0, v) < 0 else 0)
+
+
+def _e4m3_probe_values():
+    _, vals = _e4m3_table()
+    mags = np.unique(np.abs(vals))
+    mids = (mags[:-1] + mags[1:]) / 2
+    probes = [mags, mids, np.nextafter(mids.astype(np.float32), np.float32(0)),
+              np.nextafter(mids.astype(np.float32), np.float32(1e9))]
+    rng = np.random.default_rng(8)
+    probes.append(np.exp(rng.uniform(np.log(2.0 ** -12), np.log(448.0), 3000)))
+    probes.append(np.array([448.0, 449.0, 463.9, 464.0, 470.0, 0.0]))
+    p = np.concatenate([np.asarray(x, np.float64) for x in probes]).astype(np.float32)
+    return np.concatenate([p, -p])
+
+
+def test_e4m3_encode_matches_torch_and_brute_force(orc):
+    v = _e4m3_probe_values()
+    ours = np.array([orc.float_to_e4m3(float(x)) for x in v], dtype=np.uint8)
+    in_range = np.abs(v) <= 448.0  # torch turns overflow into NaN; the oracle saturates
+    theirs = torch.from_numpy(v[in_range]).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    np.testing.assert_array_equal(ours[in_range], theirs)
+    for x, c in zip(v[::7], ours[::7]):
+        assert c == _brute_force_e4m3(float(x)), x
+    # saturation and signed zero
+    assert orc.float_to_e4m3(1e30) == 0x7E and orc.float_to_e4m3(-1e30) == 0xFE
+    assert orc.float_to_e4m3(-0.0) == 0x80 and orc.float_to_e4m3(0.0) == 0x00
+
+
+def test_fp8_row_code_properties(orc):
+    rng = np.random.default_rng(9)
+    x = torch.from_numpy(rng.standard_normal((64, 512)).astype(np.float32) * 3).to(torch.bfloat16)
+    x[5] = 0.0
+    bits = x.view(torch.int16).numpy().view(np.uint16)
+    q, s = orc.quantize_rows(bits, fp8=True)
+    xf = x.float().numpy()
+    amax = np.abs(xf).max(1)
+    np.testing.assert_array_equal(s, (amax / np.float32(448.0)).astype(np.float32))
+    assert np.all(q[5] == 0) and s[5] == 0.0
+    deq = np.array([[orc.dequant_fp8(int(c), float(sc)) for c in row] for row, sc in zip(q[:8], s[:8])])
+    for r in range(8):
+        if s[r] == 0:
+            continue
+        i = int(np.argmax(np.abs(xf[r])))
+        assert q[r, i] in (0x7E, 0xFE)  # the largest magnitude takes the largest code
+        # E4M3 keeps 3 mantissa bits: relative error <= 2^-4 above 2^-6 * scale,
+        # absolute error <= 2^-10 * scale below (the subnormal spacing is 2^-9)
+        err = np.abs(deq[r] - xf[r])
+        bound = np.maximum(np.abs(xf[r]) * 2.0 ** -4, 2.0 ** -10 * s[r]) * (1 + 1e-6)
+        assert np.all(err <= bound)
+    # the code of each element is the E4M3 of fl(x / scale)
+    r = 3
+    want = [orc.float_to_e4m3(float(np.float32(v) / np.float32(s[r]))) for v in xf[r]]
+    np.testing.assert_array_equal(q[r], np.array(want, np.uint8))
+
+
+def test_fp8_payload_and_combine(orc):
+    rng = np.random.default_rng(10)
+    T, H, E, k, R = 40, 64, 8, 2, 2
+    logits = rng.standard_normal((T, E)).astype(np.float32)
+    x = torch.from_numpy(rng.standard_normal((T, H)).astype(np.float32)).to(torch.bfloat16)
+    bits = x.view(torch.int16).numpy().view(np.uint16)
+    idx, w = orc.route(logits, k, renormalize=True)
+    lay = orc.layout(idx, E, R)
+    pl, sc = orc.payload(bits, lay["row_slot"], k, 2)
+    q, s = orc.quantize_rows(bits, fp8=True)
+    tok = lay["row_slot"] // k
+    np.testing.assert_array_equal(pl, q[tok])
+    np.testing.assert_array_equal(sc, s[tok])
+    # identity experts: the combine of the FP8 payload returns each token within
+    # its rows' FP8 error (renormalised weights sum to one)
+    y = orc.combine(pl, sc, lay["slot_row"], w, T, k)
+    yf = torch.from_numpy(y.view(np.int16)).view(torch.bfloat16).float().numpy()
+    xf = x.float().numpy()
+    bound = np.abs(xf) * 2.0 ** -4 + 2.0 ** -10 * s[:, None] + np.abs(xf) * 2.0 ** -7
+    assert np.all(np.abs(yf - xf) <= bound * 1.001)
