@@ -38,6 +38,7 @@ FALLBACK_HBM_GBS = 6400.0
 L2_BYTES = 126 * 1024 * 1024
 METRIC = "dispatch+combine tokens/s and HBM GB/s as % of B300 peak (T=16384,H=4096)"
 TRAFFIC_FILE = ROOT / "profiles" / "roofline_traffic.json"
+PAYLOAD_MODE = {"bf16": 0, "int8": 1, "fp8": 2}
 
 
 # ----------------------------------------------------------------------------
@@ -47,7 +48,7 @@ def algorithmic_bytes(T, H, E, k, N, payload_int8, out_int8=False):
     """Bytes each stage must move at least once, with N dispatched rows.
 
     route:    logits T*E*4 read
-    dispatch: x T*H*2 read; payload N*H*b written (+ scales N*4 in int8)
+    dispatch: x T*H*2 read; payload N*H*b written (+ scales N*4 for int8 / FP8 codes)
     combine:  expert outputs N*H*b_out read (+ N*4 scales if int8); y T*H*2 written
     Routing metadata (indices, weights, slot maps: ~16*T*k bytes) is kept apart.
     """
@@ -216,7 +217,7 @@ def oracle_pass_seconds(w, n_tokens, payload_int8=None):
 
     ws, logits, x_bits, eo_bits = _oracle_inputs(w, n_tokens)
     orc = oracle.Oracle()
-    p8 = (w.payloads[0] == 1) if payload_int8 is None else payload_int8
+    p8 = int(w.payloads[0]) if payload_int8 is None else int(payload_int8)  # oracle payload mode
     t0 = time.perf_counter()
     orc.forward(logits, x_bits, eo_bits, ws.k, ws.R, ws.capacity_factor, ws.renormalize, p8)
     return time.perf_counter() - t0
@@ -229,7 +230,7 @@ def run_reference(args):
     from combine_warp_top_fp32_b300 import workloads
 
     w = workloads.WORKLOADS[args.workload]
-    p8 = args.payload == "int8"
+    p8 = PAYLOAD_MODE[args.payload]
     n = oracle_sample_tokens(w, target_s=args.reference_step_s)
     for _ in range(args.warmup):
         oracle_pass_seconds(w, n, p8)
@@ -264,7 +265,7 @@ def cpu_model():
 
 def workload_config(w, payload, n_rows, eager=False, path="fused"):
     rows = n_rows if n_rows is not None else w.max_rows()
-    step_bytes = algorithmic_bytes(w.T, w.H, w.E, w.k, rows, payload == "int8")["total"]
+    step_bytes = algorithmic_bytes(w.T, w.H, w.E, w.k, rows, payload != "bf16")["total"]
     l2 = (f"no flush: each step moves {step_bytes / 1e9:.2f} GB, beyond the 126 MB L2" if step_bytes > L2_BYTES else
           f"not flushed: the {step_bytes / 1e6:.1f} MB step fits in the 126 MB L2 (latency-bound shape)")
     return {"workload": w.name, "T": w.T, "H": w.H, "E": w.E, "k": w.k, "R": w.R,
@@ -292,8 +293,8 @@ def run_gpu(args):
     from combine_warp_top_fp32_b300 import workloads
 
     w = workloads.WORKLOADS[args.workload]
-    p8 = args.payload == "int8"
-    cfg = ep.config_from_workload(w, payload=ep.EP_PAYLOAD_INT8 if p8 else ep.EP_PAYLOAD_BF16)
+    p8 = PAYLOAD_MODE[args.payload]  # 0 bf16, 1 int8, 2 FP8 E4M3 (the library's EP_PAYLOAD_* values)
+    cfg = ep.config_from_workload(w, payload=p8)
     d = workloads.generate(w, device=dev)
     logits, x, eo = d["logits"], d["x"], d["expert_out"]
     buf = ep.EpBuffers.allocate(cfg)
@@ -390,7 +391,7 @@ def run_gpu(args):
     tokens = w.T * args.steps * world
     value = tokens / total_s
 
-    nb = algorithmic_bytes(w.T, w.H, w.E, w.k, N, p8)
+    nb = algorithmic_bytes(w.T, w.H, w.E, w.k, N, p8 != 0)
     nb["route+dispatch"] = nb["route"] + nb["dispatch"]
     peak, peak_src = measured_peak_gbs()
     step_gbs = nb["total"] / (ms_per_step / 1e3) / 1e9
@@ -478,7 +479,7 @@ def parse_args(argv=None):
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="capacity")
-    ap.add_argument("--payload", choices=["int8", "bf16"], default=None)
+    ap.add_argument("--payload", choices=["int8", "bf16", "fp8"], default=None)
     ap.add_argument("--path", choices=["calls", "fused"], default="fused",
                     help="fused: ep_route_dispatch + ep_combine; calls: ep_route, ep_dispatch, ep_combine")
     ap.add_argument("--no-e2e", action="store_true")

@@ -26,12 +26,13 @@ EP_ERR_DEVICE_INDEX = 5
 
 EP_PAYLOAD_BF16 = 0
 EP_PAYLOAD_INT8 = 1
+EP_PAYLOAD_FP8 = 2  # FP8 E4M3 codes (bytes) + one fp32 scale per row
 
 # Every symbol include/ep.h declares.
 EXPORTS = (
     "ep_status_string", "ep_config_check", "ep_capacity", "ep_max_rows", "ep_workspace_size",
     "ep_workspace_init", "ep_route", "ep_dispatch", "ep_combine", "ep_quantize_rows", "ep_get_error",
-    "ep_load_stats", "ep_dispatch_static", "ep_route_dispatch",
+    "ep_load_stats", "ep_dispatch_static", "ep_route_dispatch", "ep_quantize_rows_fp8",
 )
 
 
@@ -75,6 +76,7 @@ def _load():
     lib.ep_dispatch.argtypes = [CFG, P, P, P, P, P, P, P, P, P, P, P, P, SZ, P]
     lib.ep_combine.argtypes = [CFG, P, P, I32, P, P, P, P, SZ, P]
     lib.ep_quantize_rows.argtypes = [P, I64, I32, P, P, P]
+    lib.ep_quantize_rows_fp8.argtypes = [P, I64, I32, P, P, P]
     lib.ep_get_error.argtypes = [P, SZ, P]
     lib.ep_load_stats.argtypes = [P, I32, ctypes.POINTER(ep_load_stats_t)]
     lib.ep_dispatch_static.argtypes = [CFG, P, P, P, P, P, P, P, P, P, P, P, P]
@@ -106,6 +108,21 @@ def config_from_workload(w, payload=None, renormalize=None) -> ep_config_t:
     return make_config(w.T, w.H, w.E, w.k, w.R, w.capacity_factor,
                        w.renormalize if renormalize is None else renormalize,
                        w.payloads[0] if payload is None else payload)
+
+
+# bf16 rows, int8 codes, FP8 E4M3 codes (as bytes or as torch.float8_e4m3fn)
+_PAYLOAD_DTYPES = (torch.bfloat16, torch.int8, torch.uint8, torch.float8_e4m3fn)
+
+
+def payload_kind(t: torch.Tensor) -> int:
+    """EP_PAYLOAD_* of a payload / expert-output tensor from its dtype."""
+    if t.dtype == torch.bfloat16:
+        return EP_PAYLOAD_BF16
+    if t.dtype == torch.int8:
+        return EP_PAYLOAD_INT8
+    if t.dtype in (torch.uint8, torch.float8_e4m3fn):
+        return EP_PAYLOAD_FP8
+    raise ValueError(f"unsupported payload dtype {t.dtype}")
 
 
 def _ptr(t: torch.Tensor | None, dtype=None, what=""):
@@ -174,7 +191,7 @@ def ep_route(cfg, logits, topk_idx, topk_w, stream=None):
 def ep_dispatch(cfg, x, topk_idx, payload, scales, row_slot, slot_row, expert_counts, expert_raw, expert_off,
                 rank_off, n_dropped, ws, stream=None):
     _check(lib.ep_dispatch(ctypes.byref(cfg), _ptr(x, torch.bfloat16, "x"), _ptr(topk_idx, torch.int32, "topk_idx"),
-                           _ptr(payload, (torch.bfloat16, torch.int8), "payload"),
+                           _ptr(payload, _PAYLOAD_DTYPES, "payload"),
                            _ptr(scales, torch.float32, "scales"), _ptr(row_slot, torch.int32, "row_slot"),
                            _ptr(slot_row, torch.int32, "slot_row"), _ptr(expert_counts, torch.int32, "expert_counts"),
                            _ptr(expert_raw, torch.int32, "expert_raw"), _ptr(expert_off, torch.int32, "expert_off"),
@@ -187,7 +204,7 @@ def ep_route_dispatch(cfg, logits, x, topk_idx, topk_w, payload, scales, row_slo
     _check(lib.ep_route_dispatch(ctypes.byref(cfg), _ptr(logits, torch.float32, "logits"),
                                  _ptr(x, torch.bfloat16, "x"), _ptr(topk_idx, torch.int32, "topk_idx"),
                                  _ptr(topk_w, torch.float32, "topk_w"),
-                                 _ptr(payload, (torch.bfloat16, torch.int8), "payload"),
+                                 _ptr(payload, _PAYLOAD_DTYPES, "payload"),
                                  _ptr(scales, torch.float32, "scales"), _ptr(row_slot, torch.int32, "row_slot"),
                                  _ptr(slot_row, torch.int32, "slot_row"),
                                  _ptr(expert_counts, torch.int32, "expert_counts"),
@@ -198,7 +215,7 @@ def ep_route_dispatch(cfg, logits, x, topk_idx, topk_w, payload, scales, row_slo
 
 
 def ep_combine(cfg, expert_out, out_scales, out_payload, slot_row, topk_w, y, ws, stream=None):
-    _check(lib.ep_combine(ctypes.byref(cfg), _ptr(expert_out, (torch.bfloat16, torch.int8), "expert_out"),
+    _check(lib.ep_combine(ctypes.byref(cfg), _ptr(expert_out, _PAYLOAD_DTYPES, "expert_out"),
                           _ptr(out_scales, torch.float32, "out_scales"), int(out_payload),
                           _ptr(slot_row, torch.int32, "slot_row"), _ptr(topk_w, torch.float32, "topk_w"),
                           _ptr(y, torch.bfloat16, "y"), _ptr(ws, what="ws"), ws.numel() * ws.element_size(),
@@ -209,6 +226,13 @@ def ep_quantize_rows(inp, q, scales, stream=None):
     n, H = inp.shape
     _check(lib.ep_quantize_rows(_ptr(inp, torch.bfloat16, "in"), int(n), int(H), _ptr(q, torch.int8, "q"),
                                 _ptr(scales, torch.float32, "scales"), _stream(stream)), "ep_quantize_rows")
+
+
+def ep_quantize_rows_fp8(inp, q, scales, stream=None):
+    n, H = inp.shape
+    _check(lib.ep_quantize_rows_fp8(_ptr(inp, torch.bfloat16, "in"), int(n), int(H),
+                                    _ptr(q, (torch.uint8, torch.float8_e4m3fn), "q"),
+                                    _ptr(scales, torch.float32, "scales"), _stream(stream)), "ep_quantize_rows_fp8")
 
 
 def ep_get_error(ws, stream=None) -> int:
@@ -238,14 +262,15 @@ class EpBuffers:
     def allocate(cfg: ep_config_t, device="cuda", stream=None) -> "EpBuffers":
         T, H, E, k, R = cfg.T, cfg.H, cfg.E, cfg.k, cfg.R
         rows = ep_max_rows(cfg)
-        int8 = cfg.payload == EP_PAYLOAD_INT8
+        coded = cfg.payload != EP_PAYLOAD_BF16
+        pdtype = {EP_PAYLOAD_BF16: torch.bfloat16, EP_PAYLOAD_INT8: torch.int8, EP_PAYLOAD_FP8: torch.uint8}[cfg.payload]
         i32 = dict(dtype=torch.int32, device=device)
         b = EpBuffers(
             cfg=cfg,
             topk_idx=torch.empty((T, k), **i32),
             topk_w=torch.empty((T, k), dtype=torch.float32, device=device),
-            payload=torch.empty((rows, H), dtype=torch.int8 if int8 else torch.bfloat16, device=device),
-            scales=torch.empty((rows,), dtype=torch.float32, device=device) if int8 else None,
+            payload=torch.empty((rows, H), dtype=pdtype, device=device),
+            scales=torch.empty((rows,), dtype=torch.float32, device=device) if coded else None,
             row_slot=torch.empty((rows,), **i32),
             slot_row=torch.empty((T * k,), **i32),
             expert_counts=torch.empty((E,), **i32),
@@ -274,7 +299,7 @@ class EpBuffers:
                           self.n_dropped, self.ws, stream)
 
     def combine(self, expert_out, out_scales=None, stream=None):
-        out_payload = EP_PAYLOAD_INT8 if expert_out.dtype == torch.int8 else EP_PAYLOAD_BF16
+        out_payload = payload_kind(expert_out)
         ep_combine(self.cfg, expert_out, out_scales, out_payload, self.slot_row, self.topk_w, self.y, self.ws, stream)
 
     def step(self, logits, x, expert_out, out_scales=None, stream=None):

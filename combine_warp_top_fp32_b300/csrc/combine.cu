@@ -30,21 +30,33 @@ namespace {
 
 constexpr unsigned kFull = 0xffffffffu;
 
-// Bytes of one 16-byte chunk: 8 bf16 or 16 int8 elements.
-template <bool INT8>
+// Elements of one 16-byte chunk: 8 bf16, or 16 int8 / E4M3 codes.
+template <int FMT>
 struct Chunk {
-  static constexpr int kElems = INT8 ? 16 : 8;
+  static constexpr int kElems = FMT == kFmtBf16 ? 8 : 16;
 };
 
-// acc[0..EL) += w * v for one 16-byte chunk of a kept row, in element order.
-template <bool INT8>
+// acc[0..EL) += w * v for one 16-byte chunk of a kept row, in element order;
+// v = float(bf16), or (float)code * scale with the int8 or E4M3 code widened
+// exactly.
+template <int FMT>
 __device__ __forceinline__ void fma_chunk(float* acc, uint4 v, float w, float sc) {
-  if constexpr (INT8) {
+  if constexpr (FMT == kFmtInt8) {
     const uint32_t u[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
     for (int q = 0; q < 4; ++q)
 #pragma unroll
       for (int i = 0; i < 4; ++i) acc[4 * q + i] = __fmaf_rn(w, __fmul_rn(i8_at(u[q], i), sc), acc[4 * q + i]);
+  } else if constexpr (FMT == kFmtFp8) {
+    const uint32_t u[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      float f[4];
+      e4m3x2_to_f32(u[q] & 0xffffu, f[0], f[1]);
+      e4m3x2_to_f32(u[q] >> 16, f[2], f[3]);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) acc[4 * q + i] = __fmaf_rn(w, __fmul_rn(f[i], sc), acc[4 * q + i]);
+    }
   } else {
     acc[0] = __fmaf_rn(w, bf16_lo(v.x), acc[0]);
     acc[1] = __fmaf_rn(w, bf16_hi(v.x), acc[1]);
@@ -73,7 +85,7 @@ __device__ __forceinline__ void store_bf16(char* y, const float* acc) {
 
 // Gathers the next (up to) 8 kept slots of `mask` (lowest slot first) from the
 // lanes that hold them into registers of every lane; returns how many.
-template <bool INT8>
+template <int FMT>
 __device__ __forceinline__ int gather_group(unsigned& mask, int row, float w, float sc, const char* base,
                                             int64_t row_bytes, const char* (&p)[8], float (&wv)[8],
                                             float (&sv)[8]) {
@@ -83,7 +95,7 @@ __device__ __forceinline__ int gather_group(unsigned& mask, int row, float w, fl
     const int src = mask ? __ffs(mask) - 1 : 0;  // uniform across the warp
     const int r = __shfl_sync(kFull, row, src);
     wv[i] = __shfl_sync(kFull, w, src);
-    if constexpr (INT8) sv[i] = __shfl_sync(kFull, sc, src);
+    if constexpr (FMT != kFmtBf16) sv[i] = __shfl_sync(kFull, sc, src);
     p[i] = base + static_cast<int64_t>(r < 0 ? 0 : r) * row_bytes;
     if (mask) ++n;
     mask &= mask - 1u;
@@ -93,10 +105,10 @@ __device__ __forceinline__ int gather_group(unsigned& mask, int row, float w, fl
 
 // One token's chunks with at most NS kept slots (gathered in p/wv/sv): UNR
 // chunks per lane per pass, all NS*UNR loads issued before any arithmetic.
-template <bool INT8, int NS, int UNR>
+template <int FMT, int NS, int UNR>
 __device__ __forceinline__ void combine_token(int nk, int cbeg, int nchunk, int lane, const char* const (&p)[8],
                                               const float (&wv)[8], const float (&sv)[8], char* yrow) {
-  constexpr int EL = Chunk<INT8>::kElems;
+  constexpr int EL = Chunk<FMT>::kElems;
   for (int c0 = cbeg + lane; c0 < nchunk; c0 += 32 * UNR) {
     uint4 v[UNR][NS];
 #pragma unroll
@@ -114,7 +126,7 @@ __device__ __forceinline__ void combine_token(int nk, int cbeg, int nchunk, int 
       for (int e = 0; e < EL; ++e) acc[e] = 0.f;
 #pragma unroll
       for (int i = 0; i < NS; ++i)
-        if (i < nk) fma_chunk<INT8>(acc, v[u][i], wv[i], sv[i]);
+        if (i < nk) fma_chunk<FMT>(acc, v[u][i], wv[i], sv[i]);
       if (c < nchunk) store_bf16<EL>(yrow + 2 * static_cast<int64_t>(c) * EL, acc);
     }
   }
@@ -122,14 +134,15 @@ __device__ __forceinline__ void combine_token(int nk, int cbeg, int nchunk, int 
 
 // LOADS = 16-byte loads in flight per lane: a token with few kept slots walks
 // more chunks per pass, so the bytes in flight do not shrink with drops.
-template <bool INT8, int LOADS>
+template <int FMT, int LOADS>
 __global__ void __launch_bounds__(256, 2) combine_kernel(const CombineArgs a) {
-  constexpr int EL = Chunk<INT8>::kElems;
+  constexpr int EL = Chunk<FMT>::kElems;
+  constexpr bool kCoded = FMT != kFmtBf16;
   const int lane = threadIdx.x & 31;
   const int64_t warp0 = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
   const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
   const int nchunk = a.H / EL;
-  const int64_t row_bytes = INT8 ? a.H : 2 * static_cast<int64_t>(a.H);
+  const int64_t row_bytes = kCoded ? a.H : 2 * static_cast<int64_t>(a.H);
   const char* base = static_cast<const char*>(a.expert_out);
   pdl_wait();  // slot rows, weights and expert outputs come from earlier kernels
   pdl_launch_dependents();
@@ -147,7 +160,7 @@ __global__ void __launch_bounds__(256, 2) combine_kernel(const CombineArgs a) {
         row = -1;
       }
       w = a.topk_w[s];
-      if constexpr (INT8) sc = row >= 0 ? a.out_scales[row] : 0.f;
+      if constexpr (kCoded) sc = row >= 0 ? a.out_scales[row] : 0.f;
     }
   };
 
@@ -176,13 +189,13 @@ __global__ void __launch_bounds__(256, 2) combine_kernel(const CombineArgs a) {
     float wv[8], sv[8];
     if (nk <= 8) {
       unsigned m = kept;
-      gather_group<INT8>(m, row, w, sc, base, row_bytes, p, wv, sv);
+      gather_group<FMT>(m, row, w, sc, base, row_bytes, p, wv, sv);
       if (nk <= 2)
-        combine_token<INT8, 2, LOADS / 2>(nk, cbeg, cend, lane, p, wv, sv, yrow);
+        combine_token<FMT, 2, LOADS / 2>(nk, cbeg, cend, lane, p, wv, sv, yrow);
       else if (nk <= 4)
-        combine_token<INT8, 4, LOADS / 4>(nk, cbeg, cend, lane, p, wv, sv, yrow);
+        combine_token<FMT, 4, LOADS / 4>(nk, cbeg, cend, lane, p, wv, sv, yrow);
       else
-        combine_token<INT8, 8, LOADS / 8>(nk, cbeg, cend, lane, p, wv, sv, yrow);
+        combine_token<FMT, 8, LOADS / 8>(nk, cbeg, cend, lane, p, wv, sv, yrow);
     } else {
       // k > 8 with more than 8 kept slots: groups of 8 per chunk, slot order.
       // The loop bound is warp-uniform: the gathers shuffle across all lanes.
@@ -193,14 +206,14 @@ __global__ void __launch_bounds__(256, 2) combine_kernel(const CombineArgs a) {
         for (int e = 0; e < EL; ++e) acc[e] = 0.f;
         unsigned m = kept;
         while (m) {
-          const int n = gather_group<INT8>(m, row, w, sc, base, row_bytes, p, wv, sv);
+          const int n = gather_group<FMT>(m, row, w, sc, base, row_bytes, p, wv, sv);
           uint4 v[8];
 #pragma unroll
           for (int i = 0; i < 8; ++i)
             v[i] = (i < n && c < cend) ? ld_stream_v4(p[i] + 16 * static_cast<int64_t>(c)) : make_uint4(0, 0, 0, 0);
 #pragma unroll
           for (int i = 0; i < 8; ++i)
-            if (i < n) fma_chunk<INT8>(acc, v[i], wv[i], sv[i]);
+            if (i < n) fma_chunk<FMT>(acc, v[i], wv[i], sv[i]);
         }
         if (c < cend) store_bf16<EL>(yrow + 2 * static_cast<int64_t>(c) * EL, acc);
       }
@@ -208,9 +221,11 @@ __global__ void __launch_bounds__(256, 2) combine_kernel(const CombineArgs a) {
   }
 }
 
-// One row per CTA iteration; 16 elements per thread; same code as dispatch.
+// One row per CTA iteration; 16 elements per thread; the same code as the
+// dispatch (int8: scale = amax/127; FP8 E4M3: scale = amax/448).
+template <int FMT>
 __global__ void __launch_bounds__(1024) quantize_rows_kernel(const void* __restrict__ in, int64_t n, int H,
-                                                              int8_t* __restrict__ q, float* __restrict__ scales) {
+                                                              uint8_t* __restrict__ q, float* __restrict__ scales) {
   __shared__ float amax_s[2][32];
   const int c = threadIdx.x;
   const bool on = c < (H >> 4);
@@ -231,23 +246,27 @@ __global__ void __launch_bounds__(1024) quantize_rows_kernel(const void* __restr
     __syncthreads();
     float am = amax_s[buf][0];
     for (int i = 1; i < nw; ++i) am = fmaxf(am, amax_s[buf][i]);
-    const float scale = __fdiv_rn(am, 127.0f);
-    if (on) st_v4(q + t * H + 16 * c, quant16_coded(a0, a1, scale, __frcp_rn(scale)));
+    const float scale = __fdiv_rn(am, CodeMax<FMT>::kValue);
+    if (on) st_v4(q + t * H + 16 * c, quant16_fmt<FMT>(a0, a1, scale, __frcp_rn(scale)));
     if (c == 0) scales[t] = scale;
     buf ^= 1;
   }
 }
 
-int g_occ_combine[4][64];
+}  // namespace
 
-template <bool INT8, int LOADS>
+namespace {
+
+int g_occ_combine[6][64];
+
+template <int FMT, int LOADS>
 cudaError_t launch_combine_t(CombineArgs a, int sms, int* cache, cudaStream_t s) {
   constexpr int kBlock = 256;
-  const int per_sm = resident_ctas(combine_kernel<INT8, LOADS>, kBlock, 0, cache);
+  const int per_sm = resident_ctas(combine_kernel<FMT, LOADS>, kBlock, 0, cache);
   const int64_t warps = static_cast<int64_t>(sms) * per_sm * (kBlock / 32);
   // Slices per token: enough work units for about eight per warp, but no
   // slice shorter than one pass of the warp over its chunks.
-  const int nchunk = INT8 ? a.H / 16 : a.H / 8;
+  const int nchunk = a.H / Chunk<FMT>::kElems;
   const int min_slice = 32 * (LOADS / 8);
   int ns = static_cast<int>((8 * warps + a.T - 1) / a.T);
   const int max_ns = nchunk / min_slice > 1 ? nchunk / min_slice : 1;
@@ -256,32 +275,38 @@ cudaError_t launch_combine_t(CombineArgs a, int sms, int* cache, cudaStream_t s)
   const int64_t blocks_needed = (units + kBlock / 32 - 1) / (kBlock / 32);
   const int64_t want = static_cast<int64_t>(sms) * per_sm;
   const int grid = static_cast<int>(blocks_needed < want ? blocks_needed : want);
-  return launch_pdl(combine_kernel<INT8, LOADS>, grid, kBlock, 0, s, a);
+  return launch_pdl(combine_kernel<FMT, LOADS>, grid, kBlock, 0, s, a);
+}
+
+template <int FMT>
+cudaError_t launch_combine_fmt(const CombineArgs& a, int sms, cudaStream_t s) {
+  // 16 loads in flight per lane once a row is long enough to keep them busy
+  const bool deep = a.H / Chunk<FMT>::kElems >= 64;
+  return deep ? launch_combine_t<FMT, 16>(a, sms, g_occ_combine[2 * FMT], s)
+              : launch_combine_t<FMT, 8>(a, sms, g_occ_combine[2 * FMT + 1], s);
 }
 
 }  // namespace
 
 cudaError_t launch_combine(const CombineArgs& a, int sms, cudaStream_t s) {
   if (a.T == 0) return cudaSuccess;
-  // 16 loads in flight per lane once a row is long enough to keep them busy
-  const int nchunk = a.int8_out ? a.H / 16 : a.H / 8;
-  const bool deep = nchunk >= 64;
-  if (a.int8_out)
-    return deep ? launch_combine_t<true, 16>(a, sms, g_occ_combine[0], s)
-                : launch_combine_t<true, 8>(a, sms, g_occ_combine[1], s);
-  return deep ? launch_combine_t<false, 16>(a, sms, g_occ_combine[2], s)
-              : launch_combine_t<false, 8>(a, sms, g_occ_combine[3], s);
+  if (a.out_fmt == kFmtFp8) return launch_combine_fmt<kFmtFp8>(a, sms, s);
+  if (a.out_fmt == kFmtInt8) return launch_combine_fmt<kFmtInt8>(a, sms, s);
+  return launch_combine_fmt<kFmtBf16>(a, sms, s);
 }
 
-cudaError_t launch_quantize_rows(const void* in, int64_t n, int H, int8_t* q, float* scales, int sms,
+cudaError_t launch_quantize_rows(const void* in, int64_t n, int H, int fmt, void* q, float* scales, int sms,
                                  cudaStream_t s) {
   if (n == 0) return cudaSuccess;
   const int block = ((H / 16 + 31) / 32) * 32;
-  static int occ[32][64];  // per block size / 32 and device
-  const int per_sm = resident_ctas(quantize_rows_kernel, block, 0, occ[block / 32 - 1]);
-  const int64_t want = static_cast<int64_t>(sms) * per_sm;
-  const int grid = static_cast<int>(n < want ? n : want);
-  return launch_pdl(quantize_rows_kernel, grid, block, 0, s, in, n, H, q, scales);
+  static int occ[2][32][64];  // per format, block size / 32 and device
+  auto go = [&](auto kernel, int which) {
+    const int per_sm = resident_ctas(kernel, block, 0, occ[which][block / 32 - 1]);
+    const int64_t want = static_cast<int64_t>(sms) * per_sm;
+    const int grid = static_cast<int>(n < want ? n : want);
+    return launch_pdl(kernel, grid, block, 0, s, in, n, H, static_cast<uint8_t*>(q), scales);
+  };
+  return fmt == kFmtFp8 ? go(quantize_rows_kernel<kFmtFp8>, 1) : go(quantize_rows_kernel<kFmtInt8>, 0);
 }
 
 }  // namespace ep

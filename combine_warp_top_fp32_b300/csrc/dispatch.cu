@@ -264,15 +264,15 @@ __device__ __forceinline__ void ld_x32(const char* p, uint4& lo, uint4& hi) {
   }
 }
 
-// int8 payload: one CTA per token in flight (grid-stride). Thread c codes the
+// int8 or FP8 payload: one CTA per token in flight (grid-stride). Thread c codes the
 // 16-element groups c and c + blockDim.x of the row, so that every warp-wide
 // store covers whole 32-byte sectors. The next token's row is loaded while
 // this one is coded; threads j < k carry slot j's row (rows pipeline above,
 // two tokens ahead). amax: exact per-thread halfword maxima, a warp max and one
-// shared-memory step; scale = amax/127 with IEEE division; the code is the
-// branch-free corrected-quotient path (quant16_coded).
-template <bool V8>
-__global__ void __launch_bounds__(512) scatter_int8_kernel(const DispatchArgs a, int tile_log2) {
+// shared-memory step; scale = amax/127 (int8) or amax/448 (FP8) with IEEE
+// division; the code is the branch-free corrected-quotient path.
+template <bool V8, int FMT>
+__global__ void __launch_bounds__(512) scatter_code_kernel(const DispatchArgs a, int tile_log2) {
   constexpr int G = 2;  // 16-element groups per thread
   __shared__ int32_t rows_s[2][32];
   __shared__ float amax_s[2][16];
@@ -332,13 +332,13 @@ __global__ void __launch_bounds__(512) scatter_int8_kernel(const DispatchArgs a,
     __syncthreads();
     float am = amax_s[buf][0];
     for (int i = 1; i < nw; ++i) am = fmaxf(am, amax_s[buf][i]);
-    const float scale = __fdiv_rn(am, 127.0f);
+    const float scale = __fdiv_rn(am, CodeMax<FMT>::kValue);
     const float inv = __frcp_rn(scale);
 #pragma unroll
     for (int g = 0; g < G; ++g) {
       const int grp = c + g * B;
       if (grp >= ngroup) break;
-      const uint4 q = quant16_coded(cur[2 * g], cur[2 * g + 1], scale, inv);
+      const uint4 q = quant16_fmt<FMT>(cur[2 * g], cur[2 * g + 1], scale, inv);
       for (int j = 0; j < a.k; ++j) {
         const int row = rows_s[buf][j];
         if (row >= 0) st_v4(static_cast<int8_t*>(a.payload) + static_cast<int64_t>(row) * a.H + 16 * grp, q);
@@ -466,18 +466,22 @@ cudaError_t launch_scan_scatter(const DispatchArgs& a, int sms, cudaStream_t s) 
   if (a.T == 0) return cudaSuccess;
 
   const int tile_log2 = __builtin_ctz(static_cast<unsigned>(a.tile));
-  if (a.int8) {
+  if (a.fmt != kFmtBf16) {
     // two 16-element groups per thread: ceil(H/32) threads per token, rounded
     // up to whole warps (>= 32 >= k)
     const int block = (((a.H / 16 + 1) / 2 + 31) / 32) * 32;
     const bool v8 = (reinterpret_cast<uintptr_t>(a.x) & 31u) == 0;  // rows are then 32-byte aligned too
-    static int occ[2][16][64];  // per load width, block size / 32, device
-    const int per_sm = v8 ? resident_ctas(scatter_int8_kernel<true>, block, 0, occ[1][block / 32 - 1])
-                          : resident_ctas(scatter_int8_kernel<false>, block, 0, occ[0][block / 32 - 1]);
-    const int64_t want = static_cast<int64_t>(sms) * per_sm;
-    const int grid = static_cast<int>(a.T < want ? a.T : want);
-    err = v8 ? launch_pdl(scatter_int8_kernel<true>, grid, block, 0, s, a, tile_log2)
-             : launch_pdl(scatter_int8_kernel<false>, grid, block, 0, s, a, tile_log2);
+    static int occ[4][16][64];  // per load width x format, block size / 32, device
+    auto go = [&](auto kernel, int which) {
+      const int per_sm = resident_ctas(kernel, block, 0, occ[which][block / 32 - 1]);
+      const int64_t want = static_cast<int64_t>(sms) * per_sm;
+      const int grid = static_cast<int>(a.T < want ? a.T : want);
+      return launch_pdl(kernel, grid, block, 0, s, a, tile_log2);
+    };
+    if (a.fmt == kFmtFp8)
+      err = v8 ? go(scatter_code_kernel<true, kFmtFp8>, 3) : go(scatter_code_kernel<false, kFmtFp8>, 2);
+    else
+      err = v8 ? go(scatter_code_kernel<true, kFmtInt8>, 1) : go(scatter_code_kernel<false, kFmtInt8>, 0);
   } else {
     constexpr int kBlock = 256;
     static int occ[64];

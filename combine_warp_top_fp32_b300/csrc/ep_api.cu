@@ -41,7 +41,8 @@ bool config_ok(const ep_config_t* c) {
   if (c->R < 1 || c->E % c->R != 0) return false;
   if (isnan(c->capacity_factor) || isinf(c->capacity_factor)) return false;
   if (c->renormalize != 0 && c->renormalize != 1) return false;
-  if (c->payload != EP_PAYLOAD_BF16 && c->payload != EP_PAYLOAD_INT8) return false;
+  if (c->payload != EP_PAYLOAD_BF16 && c->payload != EP_PAYLOAD_INT8 && c->payload != EP_PAYLOAD_FP8_E4M3)
+    return false;
   if (static_cast<int64_t>(c->T) * c->k > INT32_MAX) return false;
   return true;
 }
@@ -70,11 +71,11 @@ ep_status_t prepare_dispatch(const ep_config_t* cfg, const void* x, const int32_
                              int32_t* expert_raw, int32_t* expert_off, int32_t* rank_off, int32_t* n_dropped,
                              void* ws, size_t ws_bytes, ep::DispatchArgs* out, int* sms_out) {
   if (!config_ok(cfg)) return EP_ERR_INVALID_ARG;
-  const bool int8 = cfg->payload == EP_PAYLOAD_INT8;
+  const bool coded = cfg->payload != EP_PAYLOAD_BF16;  // int8 or FP8 code + per-row scale
   if (!expert_counts || !expert_off || !rank_off || !n_dropped) return EP_ERR_INVALID_ARG;
   if (cfg->T > 0) {
     if (!x || !topk_idx || !payload || !row_slot || !slot_row) return EP_ERR_INVALID_ARG;
-    if (int8 && !scales) return EP_ERR_INVALID_ARG;
+    if (coded && !scales) return EP_ERR_INVALID_ARG;
     if (!aligned(x, 16) || !aligned(payload, 16)) return EP_ERR_INVALID_ARG;
   }
   if (!aligned(topk_idx, 4) || !aligned(row_slot, 4) || !aligned(slot_row, 4) || !aligned(expert_counts, 4) ||
@@ -94,7 +95,7 @@ ep_status_t prepare_dispatch(const ep_config_t* cfg, const void* x, const int32_
   a.k = cfg->k;
   a.R = cfg->R;
   a.cap = capacity_of(cfg);
-  a.int8 = int8 ? 1 : 0;
+  a.fmt = cfg->payload;  // EP_PAYLOAD_* values are the kernels' format numbers
   a.x = x;
   a.topk_idx = topk_idx;
   a.payload = payload;
@@ -117,6 +118,17 @@ ep_status_t prepare_dispatch(const ep_config_t* cfg, const void* x, const int32_
   a.ntiles = L.ntiles;
   *sms_out = sms;
   return EP_OK;
+}
+
+// int8 or FP8 per-row code of n rows (ep_quantize_rows, ep_quantize_rows_fp8).
+ep_status_t quantize_rows(const void* in, int64_t n, int32_t H, int fmt, void* q, float* scales,
+                          cudaStream_t stream) {
+  if (n < 0 || H < 16 || H > kMaxH || H % 16 != 0) return EP_ERR_INVALID_ARG;
+  if (n == 0) return EP_OK;
+  if (!in || !q || !scales || !aligned(in, 16) || !aligned(q, 16) || !aligned(scales, 4)) return EP_ERR_INVALID_ARG;
+  const int sms = current_sm_count();
+  if (sms <= 0) return EP_ERR_CUDA;
+  return from_cuda(ep::launch_quantize_rows(in, n, H, fmt, q, scales, sms, stream));
 }
 
 }  // namespace
@@ -215,11 +227,12 @@ ep_status_t ep_combine(const ep_config_t* cfg, const void* expert_out, const flo
                        int32_t out_payload, const int32_t* slot_row, const float* topk_w, void* y, void* ws,
                        size_t ws_bytes, cudaStream_t stream) {
   if (!config_ok(cfg)) return EP_ERR_INVALID_ARG;
-  if (out_payload != EP_PAYLOAD_BF16 && out_payload != EP_PAYLOAD_INT8) return EP_ERR_INVALID_ARG;
+  if (out_payload != EP_PAYLOAD_BF16 && out_payload != EP_PAYLOAD_INT8 && out_payload != EP_PAYLOAD_FP8_E4M3)
+    return EP_ERR_INVALID_ARG;
   if (ws == nullptr || ws_bytes < 256 || !aligned(ws, 256)) return EP_ERR_WORKSPACE;
   if (cfg->T == 0) return EP_OK;
-  const bool int8 = out_payload == EP_PAYLOAD_INT8;
-  if (!expert_out || !slot_row || !topk_w || !y || (int8 && !out_scales)) return EP_ERR_INVALID_ARG;
+  const bool coded = out_payload != EP_PAYLOAD_BF16;
+  if (!expert_out || !slot_row || !topk_w || !y || (coded && !out_scales)) return EP_ERR_INVALID_ARG;
   if (!aligned(expert_out, 16) || !aligned(y, 16) || !aligned(slot_row, 4) || !aligned(topk_w, 4) ||
       !aligned(out_scales, 4))
     return EP_ERR_INVALID_ARG;
@@ -229,7 +242,7 @@ ep_status_t ep_combine(const ep_config_t* cfg, const void* expert_out, const flo
   a.T = cfg->T;
   a.H = cfg->H;
   a.k = cfg->k;
-  a.int8_out = int8 ? 1 : 0;
+  a.out_fmt = out_payload;
   a.max_rows = max_rows_of(cfg);
   a.expert_out = expert_out;
   a.out_scales = out_scales;
@@ -241,12 +254,12 @@ ep_status_t ep_combine(const ep_config_t* cfg, const void* expert_out, const flo
 }
 
 ep_status_t ep_quantize_rows(const void* in, int64_t n, int32_t H, int8_t* q, float* scales, cudaStream_t stream) {
-  if (n < 0 || H < 16 || H > kMaxH || H % 16 != 0) return EP_ERR_INVALID_ARG;
-  if (n == 0) return EP_OK;
-  if (!in || !q || !scales || !aligned(in, 16) || !aligned(q, 16) || !aligned(scales, 4)) return EP_ERR_INVALID_ARG;
-  const int sms = current_sm_count();
-  if (sms <= 0) return EP_ERR_CUDA;
-  return from_cuda(ep::launch_quantize_rows(in, n, H, q, scales, sms, stream));
+  return quantize_rows(in, n, H, ep::kFmtInt8, q, scales, stream);
+}
+
+ep_status_t ep_quantize_rows_fp8(const void* in, int64_t n, int32_t H, uint8_t* q, float* scales,
+                                 cudaStream_t stream) {
+  return quantize_rows(in, n, H, ep::kFmtFp8, q, scales, stream);
 }
 
 ep_status_t ep_get_error(void* ws, size_t ws_bytes, cudaStream_t stream) {

@@ -2,6 +2,7 @@
 #pragma once
 
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -168,6 +169,92 @@ __device__ __forceinline__ uint4 quant16_fast(uint4 a0, uint4 a1, float scale, f
 __device__ __forceinline__ uint4 quant16_coded(uint4 a0, uint4 a1, float scale, float inv) {
   if (scale >= kFastScaleMin) return quant16_fast(a0, a1, scale, inv);
   return quant16(a0, a1, scale);
+}
+
+// ---- per-token FP8 E4M3 code of 16 consecutive elements ----------------------
+// scale = amax / 448 (IEEE division; 448 is the largest finite E4M3 value);
+// q = E4M3 round-to-nearest-even of fl(x / scale), saturated to +-448, by the
+// hardware conversion cvt.rn.satfinite.e4m3x2.f32. The quotient is the same
+// corrected quotient q1 as for the int8 code, with x's sign: its E4M3 code
+// equals that of the IEEE quotient for every bf16 amax with amax/448 >= 2^-100
+// and every bf16 x with |x| <= amax (checked exhaustively on the host, codes
+// compared bit for bit, 1,044,457,888 signed pairs; 61,356 differ without the
+// correction) and on the GPU by the tests.
+
+// Two floats -> two E4M3 codes in one 16-bit word (lo in the low byte).
+__device__ __forceinline__ uint32_t e4m3x2_rn_sat(float lo, float hi) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+__device__ __forceinline__ uint4 quant16_fp8_ieee(uint4 a0, uint4 a1, float scale) {
+  const uint32_t w[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+  uint32_t o[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const uint32_t p0 = e4m3x2_rn_sat(__fdiv_rn(bf16_lo(w[2 * i]), scale), __fdiv_rn(bf16_hi(w[2 * i]), scale));
+    const uint32_t p1 =
+        e4m3x2_rn_sat(__fdiv_rn(bf16_lo(w[2 * i + 1]), scale), __fdiv_rn(bf16_hi(w[2 * i + 1]), scale));
+    o[i] = p0 | (p1 << 16);
+  }
+  return make_uint4(o[0], o[1], o[2], o[3]);
+}
+
+__device__ __forceinline__ uint4 quant16_fp8_fast(uint4 a0, uint4 a1, float scale, float inv) {
+  const uint64_t inv2 = f32x2_pack(__float_as_uint(inv), __float_as_uint(inv));
+  const uint64_t nsc2 = f32x2_pack(__float_as_uint(-scale), __float_as_uint(-scale));
+  const uint32_t w[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+  uint32_t pair[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const uint64_t x2 = f32x2_pack(w[i] << 16, w[i] & 0xffff0000u);
+    const uint64_t q0 = f32x2_mul(x2, inv2);
+    // the quotient takes the sign of x: the correction turns x = -0 into +0,
+    // while fl(-0 / scale) is -0 (code 0x80); every other sign is already x's
+    const uint64_t q1 = (f32x2_fma(f32x2_fma(q0, nsc2, x2), inv2, q0) & 0x7fffffff7fffffffull) |
+                        (x2 & 0x8000000080000000ull);
+    pair[i] = e4m3x2_rn_sat(__uint_as_float(static_cast<uint32_t>(q1)), __uint_as_float(static_cast<uint32_t>(q1 >> 32)));
+  }
+  return make_uint4(pair[0] | (pair[1] << 16), pair[2] | (pair[3] << 16), pair[4] | (pair[5] << 16),
+                    pair[6] | (pair[7] << 16));
+}
+
+__device__ __forceinline__ uint4 quant16_fp8_coded(uint4 a0, uint4 a1, float scale, float inv) {
+  if (scale >= kFastScaleMin) return quant16_fp8_fast(a0, a1, scale, inv);
+  if (scale == 0.0f) return make_uint4(0, 0, 0, 0);
+  return quant16_fp8_ieee(a0, a1, scale);
+}
+
+// Payload formats of the row codes.
+enum PayloadFmt : int { kFmtBf16 = 0, kFmtInt8 = 1, kFmtFp8 = 2 };
+
+// Largest code magnitude: the scale is amax / kCodeMax.
+template <int FMT>
+struct CodeMax;
+template <>
+struct CodeMax<kFmtInt8> {
+  static constexpr float kValue = 127.0f;
+};
+template <>
+struct CodeMax<kFmtFp8> {
+  static constexpr float kValue = 448.0f;
+};
+
+template <int FMT>
+__device__ __forceinline__ uint4 quant16_fmt(uint4 a0, uint4 a1, float scale, float inv) {
+  if constexpr (FMT == kFmtFp8)
+    return quant16_fp8_coded(a0, a1, scale, inv);
+  else
+    return quant16_coded(a0, a1, scale, inv);
+}
+
+// Two E4M3 codes (one 16-bit word, lo in the low byte) -> two exact floats.
+__device__ __forceinline__ void e4m3x2_to_f32(uint32_t codes16, float& lo, float& hi) {
+  uint32_t h2;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(static_cast<uint16_t>(codes16)));
+  lo = __half2float(__ushort_as_half(static_cast<unsigned short>(h2 & 0xffffu)));
+  hi = __half2float(__ushort_as_half(static_cast<unsigned short>(h2 >> 16)));
 }
 
 // max |x| over 16 bf16 (two 16-byte words). With the sign bits cleared, the

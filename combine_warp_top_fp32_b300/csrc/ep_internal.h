@@ -87,7 +87,8 @@ cudaError_t launch_route(const float* logits, int T, int E, int k, int renorm, i
                          cudaStream_t s);
 
 struct DispatchArgs {
-  int T, H, E, k, R, cap, int8;
+  int T, H, E, k, R, cap;
+  int fmt;  // payload format: kFmtBf16, kFmtInt8 or kFmtFp8
   const void* x;
   const int32_t* topk_idx;
   void* payload;
@@ -118,7 +119,8 @@ struct RouteCountArgs {
 cudaError_t launch_route_count(const RouteCountArgs& r, cudaStream_t s);
 
 struct CombineArgs {
-  int T, H, k, int8_out;
+  int T, H, k;
+  int out_fmt;  // expert-output format: kFmtBf16, kFmtInt8 or kFmtFp8
   int slices;  // work units per token (set by the launcher)
   int64_t max_rows;
   const void* expert_out;
@@ -131,7 +133,7 @@ struct CombineArgs {
 
 cudaError_t launch_combine(const CombineArgs& a, int sms, cudaStream_t s);
 
-cudaError_t launch_quantize_rows(const void* in, int64_t n, int H, int8_t* q, float* scales, int sms,
+cudaError_t launch_quantize_rows(const void* in, int64_t n, int H, int fmt, void* q, float* scales, int sms,
                                  cudaStream_t s);
 
 }  // namespace ep

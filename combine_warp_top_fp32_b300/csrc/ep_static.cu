@@ -66,11 +66,11 @@ extern "C" ep_status_t ep_dispatch_static(const ep_config_t* cfg, const void* x,
                                           int32_t* expert_counts, int32_t* expert_raw, int32_t* expert_off,
                                           int32_t* rank_off, int32_t* n_dropped, cudaStream_t stream) {
   if (ep_config_check(cfg) != EP_OK) return EP_ERR_INVALID_ARG;
-  const bool int8 = cfg->payload == EP_PAYLOAD_INT8;
+  const bool coded = cfg->payload != EP_PAYLOAD_BF16;  // int8 or FP8 code + per-row scale
   if (!expert_counts || !expert_off || !rank_off || !n_dropped) return EP_ERR_INVALID_ARG;
   if (cfg->T > 0) {
     if (!x || !topk_idx || !payload || !row_slot || !slot_row) return EP_ERR_INVALID_ARG;
-    if (int8 && !scales) return EP_ERR_INVALID_ARG;
+    if (coded && !scales) return EP_ERR_INVALID_ARG;
     if (!is_aligned(x, 16) || !is_aligned(payload, 16)) return EP_ERR_INVALID_ARG;
   }
   if (!is_aligned(topk_idx, 4) || !is_aligned(row_slot, 4) || !is_aligned(slot_row, 4) ||
@@ -99,7 +99,7 @@ extern "C" ep_status_t ep_dispatch_static(const ep_config_t* cfg, const void* x,
   int32_t cap = 0;
   if (ep_capacity(cfg, &cap) != EP_OK) return EP_ERR_INVALID_ARG;
   a.cap = cap;
-  a.int8 = int8 ? 1 : 0;
+  a.fmt = cfg->payload;
   a.x = x;
   a.topk_idx = topk_idx;
   a.payload = payload;

@@ -60,8 +60,9 @@ typedef enum {
 } ep_status_t;
 
 typedef enum {
-  EP_PAYLOAD_BF16 = 0, /* rows are the token's bf16 bytes, unchanged              */
-  EP_PAYLOAD_INT8 = 1  /* rows are the token's int8 code + one fp32 scale per row */
+  EP_PAYLOAD_BF16 = 0,     /* rows are the token's bf16 bytes, unchanged                   */
+  EP_PAYLOAD_INT8 = 1,     /* rows are the token's int8 code + one fp32 scale per row      */
+  EP_PAYLOAD_FP8_E4M3 = 2  /* rows are the token's FP8 E4M3 code + one fp32 scale per row  */
 } ep_payload_t;
 
 /*
@@ -80,7 +81,14 @@ typedef enum {
  *                    factor, typical 1.0-1.25)
  *   renormalize      0: w = full softmax probability of the chosen expert;
  *                    1: the k chosen weights are rescaled to sum to one
- *   payload          EP_PAYLOAD_BF16 or EP_PAYLOAD_INT8 for ep_dispatch
+ *   payload          EP_PAYLOAD_BF16, EP_PAYLOAD_INT8 or EP_PAYLOAD_FP8_E4M3 for
+ *                    ep_dispatch
+ * The per-token codes (ThunderEP §2.3 per-token dynamic quantisation; §5.2
+ * and the NCCL EP article §6.3 for FP8):
+ *   int8  scale = amax/127.0f, q = clamp(rint(x/scale), -127, 127)
+ *   FP8   scale = amax/448.0f, q = E4M3 round-to-nearest-even of x/scale,
+ *         saturated to +-448 (OCP E4M3: bias 7, 3 mantissa bits, no inf)
+ * with IEEE fp32 division and amax = 0 giving scale 0 and all-zero codes.
  */
 typedef struct {
   int32_t T, H, E, k, R;
@@ -131,14 +139,14 @@ ep_status_t ep_route(const ep_config_t* cfg, const float* logits, int32_t* topk_
  * §2.3; NCCL EP §3.3 sendcounts/flat sendbuff).
  *   x              [T, H] bf16 in     token hidden states
  *   topk_idx       [T, k] int32 in    k distinct expert ids per token
- *   payload        [max_rows, H] out  bf16 (EP_PAYLOAD_BF16) or int8
- *                                     (EP_PAYLOAD_INT8); rows [0, N) are
+ *   payload        [max_rows, H] out  bf16 (EP_PAYLOAD_BF16), int8
+ *                                     (EP_PAYLOAD_INT8) or E4M3 bytes
+ *                                     (EP_PAYLOAD_FP8_E4M3); rows [0, N) are
  *                                     written, N = T*k - dropped; row order is
  *                                     (expert, token), so rank r's block is
  *                                     rows [rank_off[r], rank_off[r+1])
- *   scales         [max_rows] fp32 out one scale per row (int8 only; NULL in
- *                                     bf16 mode): scale = amax/127.0f,
- *                                     q = clamp(rint(x/scale), -127, 127)
+ *   scales         [max_rows] fp32 out one scale per row (int8 and FP8; NULL
+ *                                     in bf16 mode), codes as in ep_config_t
  *   row_slot       [max_rows] int32 out row -> t*k + j, rows [0, N)
  *   slot_row       [T*k] int32 out    (t, j) -> row, or -1 if dropped
  *   expert_counts  [E] int32 out      kept copies per expert
@@ -210,16 +218,18 @@ ep_status_t ep_dispatch_static(const ep_config_t* cfg, const void* x, const int3
 
 /*
  * ep_combine — weighted top-k recombination (ThunderEP §1.3 steps 3-4).
- *   expert_out   [max_rows, H] in  bf16 (out_payload = EP_PAYLOAD_BF16) or
- *                                  int8 (EP_PAYLOAD_INT8) expert outputs,
+ *   expert_out   [max_rows, H] in  bf16 (out_payload = EP_PAYLOAD_BF16), int8
+ *                                  (EP_PAYLOAD_INT8) or E4M3 bytes
+ *                                  (EP_PAYLOAD_FP8_E4M3) expert outputs,
  *                                  row-aligned with the dispatch payload
- *   out_scales   [max_rows] fp32   per-row scales for int8 rows, else NULL
+ *   out_scales   [max_rows] fp32   per-row scales for int8 / FP8 rows, else NULL
  *   slot_row     [T*k] int32 in    from ep_dispatch (-1 = dropped slot)
  *   topk_w       [T, k] fp32 in    from ep_route
  *   y            [T, H] bf16 out   y[t] = bf16_rne(sum over j = 0..k-1 in
  *                                  order, slot not dropped, of
  *                                  fmaf(w[t,j], v_j, acc)), acc starting at 0,
  *                                  v_j = float(bf16) or (float)q * scale
+ *                                  (q the int8 or E4M3 code, widened exactly)
  *   ws, ws_bytes workspace (its status word records bad slot_row entries)
  * A token whose k slots were all dropped gets y = 0.
  */
@@ -235,6 +245,14 @@ ep_status_t ep_combine(const ep_config_t* cfg, const void* expert_out, const flo
  */
 ep_status_t ep_quantize_rows(const void* in, int64_t n, int32_t H, int8_t* q, float* scales,
                              cudaStream_t stream);
+
+/*
+ * ep_quantize_rows_fp8 — the per-token FP8 E4M3 code (scale = amax/448) of n
+ * rows, for an expert side that returns FP8 outputs; as ep_quantize_rows
+ * otherwise (q [n, H] E4M3 bytes out, 16-byte aligned).
+ */
+ep_status_t ep_quantize_rows_fp8(const void* in, int64_t n, int32_t H, uint8_t* q, float* scales,
+                                 cudaStream_t stream);
 
 /*
  * ep_get_error — synchronises `stream`, reads the workspace's status word,

@@ -25,7 +25,7 @@ def ep():
 def _declared_functions():
     text = (ROOT / "include" / "ep.h").read_text()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"\b(ep_[a-z_]+)\s*\(", text)))
+    return sorted(set(re.findall(r"\b(ep_[a-z0-9_]+)\s*\(", text)))
 
 
 def test_every_declared_symbol_is_exported(ep):

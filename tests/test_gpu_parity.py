@@ -87,10 +87,9 @@ def _full_parity(ep, orc, w, payload, renormalize=False, device_gen="cuda"):
     lay = orc.layout(idx, w.E, w.R, w.capacity_factor)
     N = lay["N"]
     _check_layout(buf, lay, N)
-    # payload: bit-exact bytes (bf16) or codes + scales (int8)
-    int8 = payload == ep.EP_PAYLOAD_INT8
-    pl, sc = orc.payload(x_bits, lay["row_slot"], w.k, int8)
-    if int8:
+    # payload: bit-exact bytes (bf16) or codes + scales (int8, FP8 E4M3)
+    pl, sc = orc.payload(x_bits, lay["row_slot"], w.k, payload)
+    if payload != ep.EP_PAYLOAD_BF16:
         np.testing.assert_array_equal(buf.payload[:N].cpu().numpy(), pl)
         np.testing.assert_array_equal(buf.scales[:N].cpu().numpy(), sc)
     else:
@@ -109,7 +108,9 @@ def _full_parity(ep, orc, w, payload, renormalize=False, device_gen="cuda"):
     return dict(N=N, dropped=lay["n_dropped"], worst_w_rel=worst_w, **stats)
 
 
-CASES = [("tiny", 0), ("decode-latency", 1), ("prefill-mid", 0), ("prefill-mid", 1), ("capacity", 1)]
+CASES = [("tiny", 0), ("decode-latency", 1), ("prefill-mid", 0), ("prefill-mid", 1), ("capacity", 1),
+         # FP8 E4M3 per-token payload (the lower-precision extension)
+         ("decode-latency", 2), ("prefill-mid", 2), ("capacity", 2)]
 
 
 @pytest.mark.parametrize("name,payload", CASES)
@@ -129,7 +130,7 @@ def test_workload_parity_renormalized(ep, orc, name):
     _full_parity(ep, orc, workloads.WORKLOADS[name], 0, renormalize=True)
 
 
-@pytest.mark.parametrize("payload", [0, 1])
+@pytest.mark.parametrize("payload", [0, 1, 2])
 def test_large_parity_sampled(ep, orc, payload):
     """T=131072, H=8192, E=256, k=8 at full size, in the bench's launch configuration.
     Routing and all layout metadata compared in full; payload rows and combined
@@ -155,11 +156,10 @@ def test_large_parity_sampled(ep, orc, payload):
     edge_rows = np.concatenate([roff[:-1], np.maximum(roff[1:] - 1, 0), [N - 1]])
     rows = np.unique(np.concatenate([rng.integers(0, N, 4096), edge_rows]))
     x_bits = _bits(x)
-    int8 = payload == ep.EP_PAYLOAD_INT8
-    pl, sc = orc.payload(x_bits, lay["row_slot"][rows], w.k, int8)
+    pl, sc = orc.payload(x_bits, lay["row_slot"][rows], w.k, payload)
     rows_d = torch.from_numpy(rows).long().cuda()
     got = buf.payload.index_select(0, rows_d)
-    if int8:
+    if payload != ep.EP_PAYLOAD_BF16:
         np.testing.assert_array_equal(got.cpu().numpy(), pl)
         np.testing.assert_array_equal(buf.scales.index_select(0, rows_d).cpu().numpy(), sc)
     else:
@@ -188,6 +188,9 @@ EDGE = [
     (1, 16, 1, 1, 1, 0.0, 0, 0, "one token, one expert, minimum H"),
     (5, 16, 3, 2, 1, 0.0, 1, 0, "int8 at minimum H: one 16-element group"),
     (700, 48, 6, 3, 3, 0.0, 1, 0, "int8 with an odd number of 16-element groups"),
+    (5, 16, 3, 2, 1, 0.0, 2, 0, "FP8 at minimum H"),
+    (1000, 64, 8, 2, 2, 0.5, 2, 1, "FP8 with drops and a ragged last tile"),
+    (777, 16384, 4, 2, 2, 0.0, 2, 0, "FP8 at maximum H"),
     (1000, 64, 8, 2, 2, 0.0, 1, 0, "ragged last tile"),
     (2500, 48, 6, 3, 3, 0.0, 0, 1, "E not a power of two, two ragged tiles"),
     (777, 16384, 4, 2, 2, 0.0, 1, 0, "maximum H"),
@@ -251,23 +254,27 @@ def test_empty_batch(ep):
     assert ep.ep_get_error(buf.ws) == ep.EP_OK
 
 
+@pytest.mark.parametrize("fmt", ["int8", "fp8"])
 @pytest.mark.parametrize("shape", ["prefill-mid", "wide"])
-def test_int8_return_path(ep, orc, shape):
-    """Expert outputs coded per row (ep_quantize_rows) then combined as int8
-    (prefill-mid: 2 KB int8 rows; wide: 8 KB int8 rows, with drops)."""
+def test_coded_return_path(ep, orc, shape, fmt):
+    """Expert outputs coded per row (ep_quantize_rows / ep_quantize_rows_fp8)
+    then combined from the codes (prefill-mid: 2 KB rows; wide: 8 KB rows,
+    with drops)."""
     from combine_warp_top_fp32_b300 import workloads
 
+    fp8 = fmt == "fp8"
     w = workloads.WORKLOADS["prefill-mid"]
     if shape == "wide":
         w = w.replace(T=1500, H=8192, capacity_factor=1.0, seed=9)
-    cfg = ep.config_from_workload(w, payload=ep.EP_PAYLOAD_INT8)
+    kind = ep.EP_PAYLOAD_FP8 if fp8 else ep.EP_PAYLOAD_INT8
+    cfg = ep.config_from_workload(w, payload=kind)
     d = workloads.generate(w, device="cuda")
     rows = w.max_rows()
-    q = torch.empty(rows, w.H, dtype=torch.int8, device="cuda")
+    q = torch.empty(rows, w.H, dtype=torch.uint8 if fp8 else torch.int8, device="cuda")
     s = torch.empty(rows, dtype=torch.float32, device="cuda")
-    ep.ep_quantize_rows(d["expert_out"], q, s)
+    (ep.ep_quantize_rows_fp8 if fp8 else ep.ep_quantize_rows)(d["expert_out"], q, s)
     torch.cuda.synchronize()
-    q_o, s_o = orc.quantize_rows(_bits(d["expert_out"]))
+    q_o, s_o = orc.quantize_rows(_bits(d["expert_out"]), fp8=fp8)
     np.testing.assert_array_equal(q.cpu().numpy(), q_o)
     np.testing.assert_array_equal(s.cpu().numpy(), s_o)
     idx, wts = orc.route(d["logits"].cpu().numpy(), w.k)
@@ -275,13 +282,13 @@ def test_int8_return_path(ep, orc, shape):
     y_orc = orc.combine(q_o, s_o, lay["slot_row"], wts, w.T, w.k)
     buf = ep.EpBuffers.allocate(cfg)
     y = torch.empty(w.T, w.H, dtype=torch.bfloat16, device="cuda")
-    ep.ep_combine(cfg, q, s, ep.EP_PAYLOAD_INT8, torch.from_numpy(lay["slot_row"]).cuda(),
-                  torch.from_numpy(wts).cuda(), y, buf.ws)
+    ep.ep_combine(cfg, q, s, kind, torch.from_numpy(lay["slot_row"]).cuda(), torch.from_numpy(wts).cuda(), y,
+                  buf.ws)
     torch.cuda.synchronize()
     np.testing.assert_array_equal(_bits(y), y_orc)
 
 
-@pytest.mark.parametrize("payload", [0, 1])
+@pytest.mark.parametrize("payload", [0, 1, 2])
 def test_identity_experts_round_trip(ep, payload):
     """combine(dispatch(x)) with identity experts and renormalised weights gives x back."""
     T, H, E, k, R = 2048, 512, 32, 4, 4
@@ -304,7 +311,11 @@ def test_identity_experts_round_trip(ep, payload):
         s_tok = np.zeros(T)
         rs = buf.row_slot.cpu().numpy()
         s_tok[rs // k] = buf.scales.cpu().numpy()
-        assert np.all(np.abs(yf - xf) <= (s_tok / 2)[:, None] * 1.0001 + bf16_ulp(xf))
+        if payload == 1:  # int8: half a code step
+            bound = (s_tok / 2)[:, None] * 1.0001
+        else:  # E4M3: 2^-4 relative above 2^-6 * scale, 2^-10 * scale below
+            bound = np.maximum(np.abs(xf) * 2.0 ** -4, (s_tok * 2.0 ** -10)[:, None]) * 1.0001
+        assert np.all(np.abs(yf - xf) <= bound + bf16_ulp(xf))
 
 
 def test_deterministic_bytes(ep):
