@@ -472,6 +472,72 @@ def run_gpu(args):
     return 0
 
 
+# ----------------------------------------------------------------------------
+# chunked pipeline (ThunderEP §2.2 overlap, §3.4 chunk sizes)
+# ----------------------------------------------------------------------------
+def run_pipeline(args):
+    """Per chunk count C: one pass = ep_route_dispatch / stand-in expert GEMM /
+    ep_combine over C chunks on two streams. Times, per step: e2e (with the
+    GEMM experts), comm (the same pipeline with identity experts: dispatch and
+    combine only) and compute (the GEMMs alone on the same chunk buffers);
+    overlap shows as e2e < comm + compute. Each is one CUDA graph of K steps."""
+    import torch
+
+    from combine_warp_top_fp32_b300 import binding as ep
+    from combine_warp_top_fp32_b300 import pipeline, workloads
+
+    torch.cuda.set_device(0)
+    w = workloads.WORKLOADS[args.workload]
+    p8 = PAYLOAD_MODE[args.payload]
+    cfg = ep.config_from_workload(w, payload=p8)
+    d = workloads.generate(w, device="cuda", expert_out=False)
+    g = torch.Generator(device="cuda").manual_seed(7)
+    weight = (torch.randn(w.H, w.H, device="cuda", generator=g) / w.H ** 0.5).to(torch.bfloat16)
+    gemm = pipeline.gemm_experts(weight)
+
+    def identity(buf):
+        if buf.payload.dtype == torch.bfloat16:
+            return buf.payload
+        return (buf.payload, buf.scales)
+
+    def timed(fn):
+        for _ in range(args.warmup):
+            fn()
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            for _ in range(args.steps):
+                fn()
+        graph.replay()
+        torch.cuda.synchronize()
+        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        t0.record()
+        graph.replay()
+        t1.record()
+        torch.cuda.synchronize()
+        return t0.elapsed_time(t1) / args.steps
+
+    table = {}
+    for C in [int(c) for c in args.pipeline.split(",")]:
+        pipe = pipeline.ChunkedPipeline(cfg, C)
+        e2e = timed(lambda: pipe.run(d["logits"], d["x"], gemm))
+        comm = timed(lambda: pipe.run(d["logits"], d["x"], identity))
+        compute = timed(lambda: [gemm(ch.buf) for ch in pipe.chunks])
+        for ch in pipe.chunks:
+            assert ep.ep_get_error(ch.buf.ws) == ep.EP_OK
+        table[str(C)] = {"chunks": len(pipe.chunks), "e2e_ms": e2e, "comm_ms": comm, "compute_ms": compute,
+                         "overlap_saved_ms": comm + compute - e2e}
+        del pipe
+    best = min(table.values(), key=lambda r: r["e2e_ms"])
+    line = {"metric": "chunked dispatch + expert GEMM + combine, ms per step", "value": best["e2e_ms"],
+            "unit": "ms", "higher_is_better": False, "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+            "data": "synthetic", "config": dict(workload_config(w, args.payload, None, False, "fused"),
+                                                expert="one bf16 [H, H] GEMM per dispatched row (cuBLAS)"),
+            "pipeline": table}
+    print(json.dumps(line))
+    return 0
+
+
 def parse_args(argv=None):
     ap = argparse.ArgumentParser(description="MoE dispatch+combine benchmark")
     ap.add_argument("--gpus", type=int, default=1)
@@ -482,6 +548,8 @@ def parse_args(argv=None):
     ap.add_argument("--payload", choices=["int8", "bf16", "fp8"], default=None)
     ap.add_argument("--path", choices=["calls", "fused"], default="fused",
                     help="fused: ep_route_dispatch + ep_combine; calls: ep_route, ep_dispatch, ep_combine")
+    ap.add_argument("--pipeline", default=None,
+                    help="comma-separated chunk counts: time the chunked pipeline with stand-in GEMM experts")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--eager", action="store_true", help="launch through the binding each step (no CUDA graph)")
     ap.add_argument("--e2e-steps", type=int, default=10)
@@ -503,6 +571,8 @@ def main(argv=None):
     args = parse_args(argv)
     if args.impl == "reference":
         return run_reference(args)
+    if args.pipeline:
+        return run_pipeline(args)
     return run_gpu(args)
 
 
