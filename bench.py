@@ -538,6 +538,63 @@ def run_pipeline(args):
     return 0
 
 
+# ----------------------------------------------------------------------------
+# compact routing metadata (intelliparadigm §4.1: [bitmap, data])
+# ----------------------------------------------------------------------------
+def run_bitmap(args):
+    """Metadata bytes per step as (expert id, position) pairs against one
+    bitmap per token, and the device time of ep_bitmap_encode (sender) and
+    ep_bitmap_layout (receiver rebuilding counts, offsets and row -> token),
+    each one CUDA graph of K calls."""
+    import torch
+
+    from combine_warp_top_fp32_b300 import binding as ep
+    from combine_warp_top_fp32_b300 import workloads
+
+    torch.cuda.set_device(0)
+    w = workloads.WORKLOADS[args.workload]
+    cfg = ep.config_from_workload(w, payload=PAYLOAD_MODE[args.payload])
+    d = workloads.generate(w, device="cuda", expert_out=False)
+    buf = ep.EpBuffers.allocate(cfg)
+    buf.route(d["logits"])
+    words = ep.bitmap_words(w.E)
+    bm = torch.empty((w.T, words), dtype=torch.int32, device="cuda")
+    row_token = torch.empty((max(ep.ep_max_rows(cfg), 1),), dtype=torch.int32, device="cuda")
+    i32 = dict(dtype=torch.int32, device="cuda")
+    outs = [torch.empty(w.E, **i32), torch.empty(w.E, **i32), torch.empty(w.E + 1, **i32),
+            torch.empty(w.R + 1, **i32), torch.empty(1, **i32)]
+
+    def timed(fn):
+        for _ in range(args.warmup):
+            fn()
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            for _ in range(args.steps):
+                fn()
+        g.replay()
+        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        t0.record()
+        g.replay()
+        t1.record()
+        torch.cuda.synchronize()
+        return 1e3 * t0.elapsed_time(t1) / args.steps
+
+    enc = timed(lambda: ep.ep_bitmap_encode(cfg, buf.topk_idx, bm, buf.ws))
+    lay = timed(lambda: ep.ep_bitmap_layout(cfg, bm, row_token, *outs, buf.ws))
+    assert ep.ep_get_error(buf.ws) == ep.EP_OK
+    pairs_bytes = w.T * w.k * 8
+    bitmap_bytes = w.T * words * 4
+    line = {"metric": "routing metadata bytes per step, bitmap against (expert, position) pairs",
+            "value": bitmap_bytes, "unit": "bytes", "higher_is_better": False, "n_gpus": 1, "steps": args.steps,
+            "warmup": args.warmup, "data": "synthetic",
+            "config": workload_config(w, args.payload, None, False, "fused"),
+            "bitmap": {"pairs_bytes": pairs_bytes, "bitmap_bytes": bitmap_bytes,
+                       "saved_frac": 1 - bitmap_bytes / pairs_bytes, "encode_us": enc, "layout_us": lay}}
+    print(json.dumps(line))
+    return 0
+
+
 def parse_args(argv=None):
     ap = argparse.ArgumentParser(description="MoE dispatch+combine benchmark")
     ap.add_argument("--gpus", type=int, default=1)
@@ -550,6 +607,8 @@ def parse_args(argv=None):
                     help="fused: ep_route_dispatch + ep_combine; calls: ep_route, ep_dispatch, ep_combine")
     ap.add_argument("--pipeline", default=None,
                     help="comma-separated chunk counts: time the chunked pipeline with stand-in GEMM experts")
+    ap.add_argument("--bitmap", action="store_true",
+                    help="report the bitmap routing metadata (bytes saved, encode and layout times)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--eager", action="store_true", help="launch through the binding each step (no CUDA graph)")
     ap.add_argument("--e2e-steps", type=int, default=10)
@@ -573,6 +632,8 @@ def main(argv=None):
         return run_reference(args)
     if args.pipeline:
         return run_pipeline(args)
+    if args.bitmap:
+        return run_bitmap(args)
     return run_gpu(args)
 
 

@@ -32,7 +32,8 @@ EP_PAYLOAD_FP8 = 2  # FP8 E4M3 codes (bytes) + one fp32 scale per row
 EXPORTS = (
     "ep_status_string", "ep_config_check", "ep_capacity", "ep_max_rows", "ep_workspace_size",
     "ep_workspace_init", "ep_route", "ep_dispatch", "ep_combine", "ep_quantize_rows", "ep_get_error",
-    "ep_load_stats", "ep_dispatch_static", "ep_route_dispatch", "ep_quantize_rows_fp8",
+    "ep_load_stats", "ep_dispatch_static", "ep_route_dispatch", "ep_quantize_rows_fp8", "ep_bitmap_encode",
+    "ep_bitmap_layout",
 )
 
 
@@ -77,6 +78,8 @@ def _load():
     lib.ep_combine.argtypes = [CFG, P, P, I32, P, P, P, P, SZ, P]
     lib.ep_quantize_rows.argtypes = [P, I64, I32, P, P, P]
     lib.ep_quantize_rows_fp8.argtypes = [P, I64, I32, P, P, P]
+    lib.ep_bitmap_encode.argtypes = [CFG, P, P, P, SZ, P]
+    lib.ep_bitmap_layout.argtypes = [CFG, P, P, P, P, P, P, P, P, SZ, P]
     lib.ep_get_error.argtypes = [P, SZ, P]
     lib.ep_load_stats.argtypes = [P, I32, ctypes.POINTER(ep_load_stats_t)]
     lib.ep_dispatch_static.argtypes = [CFG, P, P, P, P, P, P, P, P, P, P, P, P]
@@ -233,6 +236,28 @@ def ep_quantize_rows_fp8(inp, q, scales, stream=None):
     _check(lib.ep_quantize_rows_fp8(_ptr(inp, torch.bfloat16, "in"), int(n), int(H),
                                     _ptr(q, (torch.uint8, torch.float8_e4m3fn), "q"),
                                     _ptr(scales, torch.float32, "scales"), _stream(stream)), "ep_quantize_rows_fp8")
+
+
+def bitmap_words(E: int) -> int:
+    """32-bit words per token of an expert bitmap."""
+    return (int(E) + 31) // 32
+
+
+def ep_bitmap_encode(cfg, topk_idx, bitmap, ws, stream=None):
+    _check(lib.ep_bitmap_encode(ctypes.byref(cfg), _ptr(topk_idx, torch.int32, "topk_idx"),
+                                _ptr(bitmap, (torch.int32, torch.uint32), "bitmap"), _ptr(ws, what="ws"),
+                                ws.numel() * ws.element_size(), _stream(stream)), "ep_bitmap_encode")
+
+
+def ep_bitmap_layout(cfg, bitmap, row_token, expert_counts, expert_raw, expert_off, rank_off, n_dropped, ws,
+                     stream=None):
+    _check(lib.ep_bitmap_layout(ctypes.byref(cfg), _ptr(bitmap, (torch.int32, torch.uint32), "bitmap"),
+                                _ptr(row_token, torch.int32, "row_token"),
+                                _ptr(expert_counts, torch.int32, "expert_counts"),
+                                _ptr(expert_raw, torch.int32, "expert_raw"),
+                                _ptr(expert_off, torch.int32, "expert_off"), _ptr(rank_off, torch.int32, "rank_off"),
+                                _ptr(n_dropped, torch.int32, "n_dropped"), _ptr(ws, what="ws"),
+                                ws.numel() * ws.element_size(), _stream(stream)), "ep_bitmap_layout")
 
 
 def ep_get_error(ws, stream=None) -> int:

@@ -27,12 +27,14 @@
 //            group. bf16: one warp per token, each 16-byte chunk of x loaded
 //            once and stored to every kept row.
 #include "ep_internal.h"
+#include "pairs.cuh"
 
 namespace ep {
 namespace {
 
-__global__ void __launch_bounds__(512) count_kernel(const int32_t* __restrict__ idx, int T, int E, int k, int tile,
-                                                    int ntiles, int32_t* __restrict__ tile_counts,
+template <class Pairs>
+__global__ void __launch_bounds__(512) count_kernel(const Pairs src, int T, int E, int k, int tile, int ntiles,
+                                                    int32_t* __restrict__ tile_counts,
                                                     int32_t* __restrict__ lrank, uint32_t* status,
                                                     uint32_t* ticket) {
   extern __shared__ uint32_t smem[];
@@ -51,12 +53,13 @@ __global__ void __launch_bounds__(512) count_kernel(const int32_t* __restrict__ 
   const int64_t base = t0 * k;
   const int npairs = nt * k;
   for (int p = threadIdx.x; p < npairs; p += blockDim.x) {
-    const int e = idx[base + p];
+    const int tl = p / k;
+    const int e = src.expert(t0 + tl, p - tl * k);
+    if (p - tl * k == 0 && !src.count_ok(t0 + tl)) raise_status(status, kStatusBadIndex);
     if (static_cast<unsigned>(e) >= static_cast<unsigned>(E)) {
       raise_status(status, kStatusBadIndex);
       continue;
     }
-    const int tl = p / k;
     const uint32_t bit = 1u << (tl & 31);
     const uint32_t old = atomicOr(&mask[e * TW + (tl >> 5)], bit);
     if (old & bit) raise_status(status, kStatusBadIndex);  // expert repeated within one token
@@ -74,10 +77,11 @@ __global__ void __launch_bounds__(512) count_kernel(const int32_t* __restrict__ 
   __syncthreads();
 
   for (int p = threadIdx.x; p < npairs; p += blockDim.x) {
-    const int e = idx[base + p];
+    const int tl0 = p / k;
+    const int e = src.expert(t0 + tl0, p - tl0 * k);
     int r = -1;
     if (static_cast<unsigned>(e) < static_cast<unsigned>(E)) {
-      const int tl = p / k;
+      const int tl = tl0;
       const int w = tl >> 5;
       r = static_cast<int>(pre[e * TW + w]) + __popc(mask[e * TW + w] & ((1u << (tl & 31)) - 1u));
     }
@@ -433,35 +437,51 @@ __global__ void __launch_bounds__(256) scatter_bf16_kernel(const DispatchArgs a,
 
 int count_smem_bytes(int E, int tile) { return 2 * E * (tile / 32) * static_cast<int>(sizeof(uint32_t)); }
 
-int g_count_smem_set[64];  // per device: largest dynamic shared size already allowed
 
 }  // namespace
 
-cudaError_t launch_dispatch(const DispatchArgs& a, int sms, cudaStream_t s) {
-  cudaError_t err;
-  // count: also clears the scan's ticket, so it runs even for an empty batch
+// The counting kernel for one pair source; it also clears the scan's ticket,
+// so it runs (one CTA) even for an empty batch.
+template <class Pairs>
+cudaError_t launch_count(const DispatchArgs& a, const Pairs& src, cudaStream_t s) {
+  static int smem_set[64];  // per device: largest dynamic shared size already allowed
   const int smem = count_smem_bytes(a.E, a.tile);
   if (smem > 48 * 1024) {
     int dev = 0;
-    if ((err = cudaGetDevice(&dev)) != cudaSuccess) return err;
-    if (dev >= 64 || g_count_smem_set[dev] < smem) {
-      err = cudaFuncSetAttribute(count_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    cudaError_t err = cudaGetDevice(&dev);
+    if (err != cudaSuccess) return err;
+    if (dev >= 64 || smem_set[dev] < smem) {
+      err = cudaFuncSetAttribute(count_kernel<Pairs>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
       if (err != cudaSuccess) return err;
-      if (dev < 64) g_count_smem_set[dev] = smem;
+      if (dev < 64) smem_set[dev] = smem;
     }
   }
   int cblock = ((a.tile * a.k + 31) / 32) * 32;
   cblock = cblock < 64 ? 64 : (cblock > 512 ? 512 : cblock);
-  err = launch_pdl(count_kernel, a.ntiles > 0 ? a.ntiles : 1, cblock, static_cast<size_t>(smem), s, a.topk_idx, a.T,
-                   a.E, a.k, a.tile, a.ntiles, a.tile_counts, a.lrank, a.status, a.ticket);
+  return launch_pdl(count_kernel<Pairs>, a.ntiles > 0 ? a.ntiles : 1, cblock, static_cast<size_t>(smem), s, src, a.T,
+                    a.E, a.k, a.tile, a.ntiles, a.tile_counts, a.lrank, a.status, a.ticket);
+}
+
+cudaError_t launch_scan(const DispatchArgs& a, cudaStream_t s) {
+  return launch_pdl(scan_kernel, (a.E + kScanWarps - 1) / kScanWarps, 32 * kScanWarps, 0, s, a.tile_counts, a.E,
+                    a.R, a.ntiles, a.cap, a.tile_base, a.expert_counts, a.expert_raw, a.expert_off, a.rank_off,
+                    a.n_dropped, a.kept, a.dropped, a.ticket);
+}
+
+cudaError_t launch_dispatch(const DispatchArgs& a, int sms, cudaStream_t s) {
+  const cudaError_t err = launch_count(a, IdxPairs{a.topk_idx, a.k}, s);
   if (err != cudaSuccess) return err;
   return launch_scan_scatter(a, sms, s);
 }
 
+cudaError_t launch_layout_from_bitmap(const DispatchArgs& a, const uint32_t* bitmap, int words, cudaStream_t s) {
+  const cudaError_t err = launch_count(a, BitmapPairs{bitmap, words, a.k}, s);
+  if (err != cudaSuccess) return err;
+  return launch_scan(a, s);
+}
+
 cudaError_t launch_scan_scatter(const DispatchArgs& a, int sms, cudaStream_t s) {
-  cudaError_t err = launch_pdl(scan_kernel, (a.E + kScanWarps - 1) / kScanWarps, 32 * kScanWarps, 0, s,
-                               a.tile_counts, a.E, a.R, a.ntiles, a.cap, a.tile_base, a.expert_counts, a.expert_raw,
-                               a.expert_off, a.rank_off, a.n_dropped, a.kept, a.dropped, a.ticket);
+  cudaError_t err = launch_scan(a, s);
   if (err != cudaSuccess) return err;
   if (a.T == 0) return cudaSuccess;
 

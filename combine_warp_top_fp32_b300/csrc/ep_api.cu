@@ -64,6 +64,10 @@ int64_t max_rows_of(const ep_config_t* c) {
 
 ep_status_t from_cuda(cudaError_t e) { return e == cudaSuccess ? EP_OK : EP_ERR_CUDA; }
 
+ep_status_t carve_layout(const ep_config_t* cfg, int32_t* expert_counts, int32_t* expert_raw, int32_t* expert_off,
+                         int32_t* rank_off, int32_t* n_dropped, void* ws, size_t ws_bytes, ep::DispatchArgs* out,
+                         int* sms_out);
+
 // Checks the dispatch arguments (before any launch) and fills the kernel
 // arguments, with the workspace carved into its regions.
 ep_status_t prepare_dispatch(const ep_config_t* cfg, const void* x, const int32_t* topk_idx, void* payload,
@@ -82,6 +86,24 @@ ep_status_t prepare_dispatch(const ep_config_t* cfg, const void* x, const int32_
       !aligned(expert_raw, 4) || !aligned(expert_off, 4) || !aligned(rank_off, 4) || !aligned(n_dropped, 4) ||
       !aligned(scales, 4))
     return EP_ERR_INVALID_ARG;
+  const ep_status_t st = carve_layout(cfg, expert_counts, expert_raw, expert_off, rank_off, n_dropped, ws, ws_bytes,
+                                      out, sms_out);
+  if (st != EP_OK) return st;
+  ep::DispatchArgs& a = *out;
+  a.x = x;
+  a.topk_idx = topk_idx;
+  a.payload = payload;
+  a.scales = scales;
+  a.row_slot = row_slot;
+  a.slot_row = slot_row;
+  return EP_OK;
+}
+
+// The layout part of the kernel arguments (sizes, cap, the layout outputs and
+// the workspace regions), after the workspace check.
+ep_status_t carve_layout(const ep_config_t* cfg, int32_t* expert_counts, int32_t* expert_raw, int32_t* expert_off,
+                         int32_t* rank_off, int32_t* n_dropped, void* ws, size_t ws_bytes, ep::DispatchArgs* out,
+                         int* sms_out) {
   const ep::WsLayout L = ep::ws_layout(cfg->T, cfg->E, cfg->k);
   if (ws == nullptr || ws_bytes < L.total || !aligned(ws, 256)) return EP_ERR_WORKSPACE;
   const int sms = current_sm_count();
@@ -96,12 +118,12 @@ ep_status_t prepare_dispatch(const ep_config_t* cfg, const void* x, const int32_
   a.R = cfg->R;
   a.cap = capacity_of(cfg);
   a.fmt = cfg->payload;  // EP_PAYLOAD_* values are the kernels' format numbers
-  a.x = x;
-  a.topk_idx = topk_idx;
-  a.payload = payload;
-  a.scales = scales;
-  a.row_slot = row_slot;
-  a.slot_row = slot_row;
+  a.x = nullptr;
+  a.topk_idx = nullptr;
+  a.payload = nullptr;
+  a.scales = nullptr;
+  a.row_slot = nullptr;
+  a.slot_row = nullptr;
   a.expert_counts = expert_counts;
   a.expert_raw = expert_raw;
   a.expert_off = expert_off;
@@ -221,6 +243,35 @@ ep_status_t ep_route_dispatch(const ep_config_t* cfg, const float* logits, const
   const cudaError_t err = ep::launch_route_count(r, stream);
   if (err != cudaSuccess) return EP_ERR_CUDA;
   return from_cuda(ep::launch_scan_scatter(a, sms, stream));
+}
+
+ep_status_t ep_bitmap_encode(const ep_config_t* cfg, const int32_t* topk_idx, uint32_t* bitmap, void* ws,
+                             size_t ws_bytes, cudaStream_t stream) {
+  if (!config_ok(cfg)) return EP_ERR_INVALID_ARG;
+  if (ws == nullptr || ws_bytes < 256 || !aligned(ws, 256)) return EP_ERR_WORKSPACE;
+  if (cfg->T == 0) return EP_OK;
+  if (!topk_idx || !bitmap || !aligned(topk_idx, 4) || !aligned(bitmap, 4)) return EP_ERR_INVALID_ARG;
+  const int sms = current_sm_count();
+  if (sms <= 0) return EP_ERR_CUDA;
+  return from_cuda(ep::launch_encode_bitmap(topk_idx, cfg->T, cfg->E, cfg->k, bitmap, static_cast<uint32_t*>(ws), sms,
+                                            stream));
+}
+
+ep_status_t ep_bitmap_layout(const ep_config_t* cfg, const uint32_t* bitmap, int32_t* row_token,
+                             int32_t* expert_counts, int32_t* expert_raw, int32_t* expert_off, int32_t* rank_off,
+                             int32_t* n_dropped, void* ws, size_t ws_bytes, cudaStream_t stream) {
+  if (!config_ok(cfg)) return EP_ERR_INVALID_ARG;
+  if (!expert_counts || !expert_off || !rank_off || !n_dropped) return EP_ERR_INVALID_ARG;
+  if (cfg->T > 0 && (!bitmap || !row_token)) return EP_ERR_INVALID_ARG;
+  if (!aligned(bitmap, 4) || !aligned(row_token, 4) || !aligned(expert_counts, 4) || !aligned(expert_raw, 4) ||
+      !aligned(expert_off, 4) || !aligned(rank_off, 4) || !aligned(n_dropped, 4))
+    return EP_ERR_INVALID_ARG;
+  ep::DispatchArgs a;
+  int sms = 0;
+  const ep_status_t st =
+      carve_layout(cfg, expert_counts, expert_raw, expert_off, rank_off, n_dropped, ws, ws_bytes, &a, &sms);
+  if (st != EP_OK) return st;
+  return from_cuda(ep::launch_bitmap_layout(a, bitmap, row_token, sms, stream));
 }
 
 ep_status_t ep_combine(const ep_config_t* cfg, const void* expert_out, const float* out_scales,

@@ -103,6 +103,13 @@ struct DispatchArgs {
 
 // ep_dispatch: count kernel, then scan and scatter.
 cudaError_t launch_dispatch(const DispatchArgs& a, int sms, cudaStream_t s);
+// Counts and offsets from per-token expert bitmaps [T, words] (count + scan).
+cudaError_t launch_layout_from_bitmap(const DispatchArgs& a, const uint32_t* bitmap, int words, cudaStream_t s);
+// ep_bitmap_encode / ep_bitmap_layout.
+cudaError_t launch_encode_bitmap(const int32_t* idx, int64_t T, int E, int k, uint32_t* bitmap, uint32_t* status,
+                                 int sms, cudaStream_t s);
+cudaError_t launch_bitmap_layout(const DispatchArgs& a, const uint32_t* bitmap, int32_t* row_token, int sms,
+                                 cudaStream_t s);
 // The scan and the scatter alone, once tile_counts / lrank are written (by
 // the count kernel or the fused route+count kernel) and the ticket is clear.
 cudaError_t launch_scan_scatter(const DispatchArgs& a, int sms, cudaStream_t s);

@@ -181,6 +181,38 @@ ep_status_t ep_route_dispatch(const ep_config_t* cfg, const float* logits, const
                               int32_t* n_dropped, void* ws, size_t ws_bytes, cudaStream_t stream);
 
 /*
+ * ep_bitmap_encode — compact routing metadata (MoE sparse-communication
+ * article, intelliparadigm.com, §4.1: the index of [expert, position] entries
+ * sent with each copy becomes one bitmap per token).
+ *   topk_idx  [T, k] int32 in    k distinct expert ids per token
+ *   bitmap    [T, W] uint32 out  W = (E + 31) / 32; bit e % 32 of word e / 32
+ *                                is set iff the token chose expert e
+ *   ws        workspace (its status word records out-of-range or repeated ids)
+ * 4*W bytes per token take the place of k (expert id, position) pairs of
+ * 4 + 4 bytes (E = 128, k = 8: 16 bytes against 64).
+ */
+ep_status_t ep_bitmap_encode(const ep_config_t* cfg, const int32_t* topk_idx, uint32_t* bitmap, void* ws,
+                             size_t ws_bytes, cudaStream_t stream);
+
+/*
+ * ep_bitmap_layout — what a receiving rank rebuilds from the bitmaps alone:
+ * the same expert_counts, expert_raw (may be NULL), expert_off, rank_off and
+ * n_dropped as ep_dispatch, and row_token[row] = the source token of each of
+ * the rows [0, N) of the rank-major buffer (ep_dispatch's row_slot[row] / k).
+ * The layout depends only on which experts each token chose (rows within an
+ * expert are in token order, the cap drops the latest tokens), not on the
+ * slot order, so nothing else has to travel with the data.
+ *   bitmap     [T, W] uint32 in   each token with exactly k bits set (fewer,
+ *                                 more, or bits at or above E set
+ *                                 EP_ERR_DEVICE_INDEX in the status word)
+ *   row_token  [max_rows] int32 out
+ *   ws         workspace from ep_workspace_size(), initialised once
+ */
+ep_status_t ep_bitmap_layout(const ep_config_t* cfg, const uint32_t* bitmap, int32_t* row_token,
+                             int32_t* expert_counts, int32_t* expert_raw, int32_t* expert_off, int32_t* rank_off,
+                             int32_t* n_dropped, void* ws, size_t ws_bytes, cudaStream_t stream);
+
+/*
  * ep_dispatch_static — ep_dispatch for callers that cannot allocate device
  * memory. The pages have no counterpart to this call: it exists only for
  * this library's users.
