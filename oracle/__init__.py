@@ -15,8 +15,8 @@ Functions and the passages they follow:
   the rank-major row order (NCCL EP article, hotelren.com, §3.3 flat sendbuff;
   ThunderEP on consumer GPUs, bjdmk.com.cn, §2.1 aggregation).
 * :func:`quantize_rows` / :func:`payload` — per-token int8 code (ThunderEP §2.3),
-  or the same per-token scheme with an FP8 E4M3 code (ThunderEP §5.2; NCCL EP
-  article §6.3).
+  or the same per-token scheme with an FP8 E4M3 or a 4-bit code (ThunderEP
+  §5.2; NCCL EP article §6.3).
 * :func:`combine` — gate-weighted sum of the k expert outputs (ThunderEP §1.3).
 """
 from __future__ import annotations
@@ -74,6 +74,10 @@ def _bind(lib):
     lib.oracle_dequant_fp8.restype = ctypes.c_float
     lib.oracle_quantize_row_fp8.argtypes = [I, P, P, P]
     lib.oracle_quantize_rows_fp8.argtypes = [I, I, P, P, P]
+    lib.oracle_quantize_row_int4.argtypes = [I, P, P, P]
+    lib.oracle_quantize_rows_int4.argtypes = [I, I, P, P, P]
+    lib.oracle_dequant_int4.argtypes = [P, I, ctypes.c_float]
+    lib.oracle_dequant_int4.restype = ctypes.c_float
     lib.oracle_float_to_e4m3.argtypes = [ctypes.c_float]
     lib.oracle_float_to_e4m3.restype = ctypes.c_uint8
     lib.oracle_e4m3_to_float.argtypes = [ctypes.c_uint8]
@@ -152,12 +156,16 @@ class Oracle:
                     slot_row=slot_row, row_slot=row_slot[:N].copy(), n_dropped=int(nd[0]), N=N)
 
     # step 5
-    def quantize_rows(self, x_bits: np.ndarray, fp8: bool = False):
-        """Per-row int8 codes (int8 array), or E4M3 codes (uint8 array) with fp8=True."""
+    def quantize_rows(self, x_bits: np.ndarray, fp8: bool = False, int4: bool = False):
+        """Per-row int8 codes (int8 array), E4M3 codes (uint8 array) with fp8=True,
+        or packed int4 codes ([n, H/2] uint8 array) with int4=True."""
         x_bits = np.ascontiguousarray(x_bits, dtype=np.uint16)
         n, H = x_bits.shape
         s = np.empty(n, np.float32)
-        if fp8:
+        if int4:
+            q = np.empty((n, H // 2), np.uint8)
+            _check(self.lib.oracle_quantize_rows_int4(n, H, _p(x_bits), _p(q), _p(s)), "quantize_rows_int4")
+        elif fp8:
             q = np.empty((n, H), np.uint8)
             _check(self.lib.oracle_quantize_rows_fp8(n, H, _p(x_bits), _p(q), _p(s)), "quantize_rows_fp8")
         else:
@@ -166,7 +174,8 @@ class Oracle:
         return q, s
 
     def payload(self, x_bits: np.ndarray, row_slot: np.ndarray, k: int, mode):
-        """mode: 0/False bf16 bytes, 1/True int8 code, 2 FP8 E4M3 code (uint8)."""
+        """mode: 0/False bf16 bytes, 1/True int8 code, 2 FP8 E4M3 code (uint8),
+        3 packed int4 code ([N, H/2] uint8)."""
         mode = int(mode)
         x_bits = np.ascontiguousarray(x_bits, dtype=np.uint16)
         row_slot = np.ascontiguousarray(row_slot, dtype=np.int32)
@@ -178,6 +187,9 @@ class Oracle:
         elif mode == 2:
             pl = np.empty((N, H), np.uint8)
             sc = np.empty(N, np.float32)
+        elif mode == 3:
+            pl = np.empty((N, H // 2), np.uint8)
+            sc = np.empty(N, np.float32)
         else:
             pl = np.empty((N, H), np.uint16)
             sc = None
@@ -186,6 +198,10 @@ class Oracle:
 
     def dequant(self, q: int, scale: float) -> float:
         return float(self.lib.oracle_dequant(int(q), float(scale)))
+
+    def dequant_int4(self, q_row: np.ndarray, h: int, scale: float) -> float:
+        q_row = np.ascontiguousarray(q_row, dtype=np.uint8)
+        return float(self.lib.oracle_dequant_int4(_p(q_row), int(h), float(scale)))
 
     def dequant_fp8(self, code: int, scale: float) -> float:
         return float(self.lib.oracle_dequant_fp8(int(code), float(scale)))
@@ -198,10 +214,11 @@ class Oracle:
 
     # step 7
     def combine(self, expert_out: np.ndarray, out_scales: np.ndarray | None, slot_row: np.ndarray,
-                topk_w: np.ndarray, T: int, k: int):
+                topk_w: np.ndarray, T: int, k: int, int4: bool = False):
+        """int4=True: expert_out is [*, H/2] packed int4 codes (uint8)."""
         expert_out = np.ascontiguousarray(expert_out)
-        H = expert_out.shape[1]
-        out_mode = _out_mode(expert_out)
+        H = expert_out.shape[1] * (2 if int4 else 1)
+        out_mode = 3 if int4 else _out_mode(expert_out)
         slot_row = np.ascontiguousarray(slot_row, dtype=np.int32).reshape(-1)
         topk_w = np.ascontiguousarray(topk_w, dtype=np.float32).reshape(-1)
         sc = None if out_scales is None else np.ascontiguousarray(out_scales, dtype=np.float32)
@@ -210,11 +227,12 @@ class Oracle:
                                        _p(topk_w), _p(y)), "combine")
         return y
 
-    def combine_tokens(self, tokens: np.ndarray, expert_out: np.ndarray, out_scales, slot_row, topk_w, k: int):
+    def combine_tokens(self, tokens: np.ndarray, expert_out: np.ndarray, out_scales, slot_row, topk_w, k: int,
+                       int4: bool = False):
         tokens = np.ascontiguousarray(tokens, dtype=np.int32)
         expert_out = np.ascontiguousarray(expert_out)
-        H = expert_out.shape[1]
-        out_mode = _out_mode(expert_out)
+        H = expert_out.shape[1] * (2 if int4 else 1)
+        out_mode = 3 if int4 else _out_mode(expert_out)
         slot_row = np.ascontiguousarray(slot_row, dtype=np.int32).reshape(-1)
         topk_w = np.ascontiguousarray(topk_w, dtype=np.float32).reshape(-1)
         sc = None if out_scales is None else np.ascontiguousarray(out_scales, dtype=np.float32)

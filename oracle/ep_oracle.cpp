@@ -22,8 +22,9 @@
 //                  by target card"; NCCL EP article §3.3)
 //   5. payload    per-token dynamic int8 quantisation, one scale per token
 //                 (ThunderEP §2.3 "per-token dynamic quantisation"); or the
-//                 same per-token scheme with an FP8 E4M3 code (ThunderEP §5.2
-//                 "lower-precision payloads"; NCCL EP article §6.3 FP8)
+//                 same per-token scheme with an FP8 E4M3 or a 4-bit code
+//                 (ThunderEP §5.2 "lower-precision payloads"; NCCL EP article
+//                 §6.3 FP8)
 //   6. dequant    v = q * scale at the receiver (ThunderEP §2.3)
 //   7. combine    gate-weighted sum of the k expert outputs back at the source
 //                 (ThunderEP §1.3, steps 3 and 4 of the EP flow; §3.3 combine)
@@ -310,6 +311,52 @@ int oracle_quantize_rows_fp8(int n, int H, const uint16_t* in, uint8_t* q, float
   return 0;
 }
 
+// ---------------------------------------------------------------------------
+// Step 5, int4 variant — the per-token scheme with 4-bit codes (ThunderEP
+// §5.2 names 4-bit payloads as the next, more aggressive compression).
+//   a     = max_h |x_h|
+//   scale = a / 7.0f                  (fp32 IEEE division)
+//   q_h   = clamp(rint(x_h / scale), -7, 7), fp32 division, ties to even
+//   byte i of the row = (q_{2i} & 0xF) | ((q_{2i+1} & 0xF) << 4)
+// Reading (pages silent): the int8 scheme with 7 in place of 127, so that -8
+// is never used and the code is symmetric; two's-complement nibbles, the
+// lower-indexed element in the low nibble; a == 0 gives scale 0 and 0 bytes.
+// ---------------------------------------------------------------------------
+int oracle_quantize_row_int4(int H, const uint16_t* x_row, uint8_t* q_row, float* scale_out) {
+  if (H < 0 || H % 2 != 0) return -1;
+  float a = 0.0f;
+  for (int h = 0; h < H; ++h) {
+    const float v = std::fabs(bf16_bits_to_float(x_row[h]));
+    if (v > a) a = v;
+  }
+  const float scale = a / 7.0f;
+  for (int i = 0; i < H / 2; ++i) {
+    int q[2] = {0, 0};
+    for (int j = 0; j < 2 && scale != 0.0f; ++j) {
+      float r = std::rint(bf16_bits_to_float(x_row[2 * i + j]) / scale);
+      if (r > 7.0f) r = 7.0f;
+      if (r < -7.0f) r = -7.0f;
+      q[j] = static_cast<int>(r);
+    }
+    q_row[i] = static_cast<uint8_t>((q[0] & 0xF) | ((q[1] & 0xF) << 4));
+  }
+  *scale_out = scale;
+  return 0;
+}
+
+int oracle_quantize_rows_int4(int n, int H, const uint16_t* in, uint8_t* q, float* scales) {
+  if (n < 0 || H < 0 || H % 2 != 0) return -1;
+  for (int i = 0; i < n; ++i)
+    oracle_quantize_row_int4(H, in + static_cast<size_t>(i) * H, q + static_cast<size_t>(i) * (H / 2), &scales[i]);
+  return 0;
+}
+
+// Element h of an int4 row: its nibble, sign-extended, times the scale.
+float oracle_dequant_int4(const uint8_t* q_row, int h, float scale) {
+  const int nib = (q_row[h / 2] >> (4 * (h % 2))) & 0xF;
+  return static_cast<float>(nib >= 8 ? nib - 16 : nib) * scale;
+}
+
 // E4M3 helpers exported for the tests' pins of the oracle's conversions.
 uint8_t oracle_float_to_e4m3(float v) { return float_to_e4m3_rne_sat(v); }
 float oracle_e4m3_to_float(uint8_t c) { return e4m3_code_to_float(c); }
@@ -318,20 +365,25 @@ float oracle_e4m3_to_float(uint8_t c) { return e4m3_code_to_float(c); }
 // Step 4+5 — the dispatch payload (ThunderEP §2.1 "aggregate by target card"
 // then §2.3 compression): every kept row is a copy of its token's x row,
 // bf16 bytes unchanged (mode 0), that token's int8 code and scale (mode 1),
-// or its FP8 E4M3 code and scale (mode 2). Rows are written from row_slot,
-// N rows. payload is [N, H] uint16 (bf16), int8 or uint8 (E4M3 codes);
-// scales is [N] (modes 1 and 2).
+// its FP8 E4M3 code and scale (mode 2), or its packed int4 code and scale
+// (mode 3). Rows are written from row_slot, N rows. payload is [N, H] uint16
+// (bf16), int8 or uint8 (E4M3 codes), or [N, H/2] uint8 (int4 pairs); scales
+// is [N] (modes 1 to 3).
 // ---------------------------------------------------------------------------
 int oracle_payload(int T, int H, int k, int N, int mode, const uint16_t* x,
                    const int32_t* row_slot, void* payload, float* scales) {
-  if (T < 0 || H < 0 || k < 1 || N < 0 || mode < 0 || mode > 2) return -1;
+  if (T < 0 || H < 0 || k < 1 || N < 0 || mode < 0 || mode > 3) return -1;
   std::vector<int8_t> q(static_cast<size_t>(H));
   for (int row = 0; row < N; ++row) {
     const int32_t s = row_slot[row];
     if (s < 0 || s >= T * k) return -2;
     const int t = s / k;
     const uint16_t* xr = x + static_cast<size_t>(t) * H;
-    if (mode == 2) {
+    if (mode == 3) {
+      float scale;
+      oracle_quantize_row_int4(H, xr, static_cast<uint8_t*>(payload) + static_cast<size_t>(row) * (H / 2), &scale);
+      scales[row] = scale;
+    } else if (mode == 2) {
       float scale;
       oracle_quantize_row_fp8(H, xr, static_cast<uint8_t*>(payload) + static_cast<size_t>(row) * H, &scale);
       scales[row] = scale;
@@ -364,12 +416,13 @@ float oracle_dequant_fp8(uint8_t q, float scale) { return e4m3_code_to_float(q) 
 // Reading: fused multiply-add per slot (the pages fix no order or rounding;
 // fixed slot order is what makes the result reproducible).
 // out_mode 0: expert_out is [*, H] bf16 bits; 1: int8 codes with
-// out_scales[*]; 2: E4M3 codes with out_scales[*].
+// out_scales[*]; 2: E4M3 codes with out_scales[*]; 3: [*, H/2] packed int4
+// codes with out_scales[*].
 // ---------------------------------------------------------------------------
 int oracle_combine(int T, int H, int k, int out_mode, const void* expert_out,
                    const float* out_scales, const int32_t* slot_row, const float* topk_w,
                    uint16_t* y) {
-  if (T < 0 || H < 0 || k < 1 || out_mode < 0 || out_mode > 2) return -1;
+  if (T < 0 || H < 0 || k < 1 || out_mode < 0 || out_mode > 3) return -1;
   for (int t = 0; t < T; ++t) {
     for (int h = 0; h < H; ++h) {
       float acc = 0.0f;
@@ -378,7 +431,10 @@ int oracle_combine(int T, int H, int k, int out_mode, const void* expert_out,
         if (row < 0) continue;
         const size_t at = static_cast<size_t>(row) * H + h;
         float v;
-        if (out_mode == 2)
+        if (out_mode == 3)
+          v = oracle_dequant_int4(static_cast<const uint8_t*>(expert_out) + static_cast<size_t>(row) * (H / 2), h,
+                                  out_scales[row]);
+        else if (out_mode == 2)
           v = oracle_dequant_fp8(static_cast<const uint8_t*>(expert_out)[at], out_scales[row]);
         else if (out_mode == 1)
           v = oracle_dequant(static_cast<const int8_t*>(expert_out)[at], out_scales[row]);
@@ -407,7 +463,10 @@ int oracle_combine_tokens(int n_tokens, const int32_t* tokens, int H, int k, int
         if (row < 0) continue;
         const size_t at = static_cast<size_t>(row) * H + h;
         float v;
-        if (out_mode == 2)
+        if (out_mode == 3)
+          v = oracle_dequant_int4(static_cast<const uint8_t*>(expert_out) + static_cast<size_t>(row) * (H / 2), h,
+                                  out_scales[row]);
+        else if (out_mode == 2)
           v = oracle_dequant_fp8(static_cast<const uint8_t*>(expert_out)[at], out_scales[row]);
         else if (out_mode == 1)
           v = oracle_dequant(static_cast<const int8_t*>(expert_out)[at], out_scales[row]);

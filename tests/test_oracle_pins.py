@@ -545,3 +545,66 @@ def test_fp8_payload_and_combine(orc):
     xf = x.float().numpy()
     bound = np.abs(xf) * 2.0 ** -4 + 2.0 ** -10 * s[:, None] + np.abs(xf) * 2.0 ** -7
     assert np.all(np.abs(yf - xf) <= bound * 1.001)
+
+
+# ----------------------------------------------------------------------------
+# 4-bit per-token payload (ThunderEP §5.2 4-bit compression): two's-complement
+# nibbles, the lower-indexed element in the low nibble, scale = amax/7.
+# ----------------------------------------------------------------------------
+def _unpack_int4(q):
+    lo = (q & 0xF).astype(np.int8)
+    hi = (q >> 4).astype(np.int8)
+    lo = np.where(lo >= 8, lo - 16, lo)
+    hi = np.where(hi >= 8, hi - 16, hi)
+    return np.stack([lo, hi], -1).reshape(q.shape[0], -1)
+
+
+def test_int4_packing_and_ties(orc):
+    # amax 7 gives scale 1 exactly, so x / scale = x: the half-integers tie and
+    # go to the even neighbour (0.5 -> 0, 1.5 -> 2, 2.5 -> 2, -1.5 -> -2)
+    x = torch.tensor([[7.0, -7.0, 0.5, 1.5, 2.5, -0.5, -1.5, 3.25] + [0.0] * 8]).to(torch.bfloat16)
+    bits = x.view(torch.int16).numpy().view(np.uint16)
+    q, s = orc.quantize_rows(bits, int4=True)
+    assert s[0] == 1.0
+    # codes 7, -7, 0, 2, 2, 0, -2, 3: bytes (q0 & 15) | (q1 & 15) << 4
+    assert q[0].tolist() == [0x97, 0x20, 0x02, 0x3E, 0, 0, 0, 0]
+    assert [orc.dequant_int4(q[0], h, s[0]) for h in range(8)] == [7.0, -7.0, 0.0, 2.0, 2.0, 0.0, -2.0, 3.0]
+
+
+def test_int4_codes_against_numpy_rint(orc):
+    rng = np.random.default_rng(12)
+    x = torch.from_numpy(rng.standard_normal((48, 256)).astype(np.float32) * 2).to(torch.bfloat16)
+    x[7] = 0.0
+    bits = x.view(torch.int16).numpy().view(np.uint16)
+    q, s = orc.quantize_rows(bits, int4=True)
+    xf = x.float().numpy()
+    scale = (np.abs(xf).max(1) / np.float32(7.0)).astype(np.float32)
+    np.testing.assert_array_equal(s, scale)
+    safe = np.where(scale > 0, scale, np.float32(1))
+    want = np.where(scale[:, None] > 0, np.clip(np.rint((xf / safe[:, None]).astype(np.float32)), -7, 7), 0)
+    np.testing.assert_array_equal(_unpack_int4(q), want.astype(np.int8))
+    # error bound and the extremes
+    deq = _unpack_int4(q).astype(np.float32) * s[:, None]
+    assert np.all(np.abs(deq - xf) <= s[:, None] / 2 * (1 + 1e-6))
+    rows = np.flatnonzero(s > 0)
+    assert np.all(np.abs(_unpack_int4(q))[rows, np.argmax(np.abs(xf[rows]), 1)] == 7)
+
+
+def test_int4_payload_and_combine(orc):
+    rng = np.random.default_rng(13)
+    T, H, E, k, R = 40, 64, 8, 2, 2
+    logits = rng.standard_normal((T, E)).astype(np.float32)
+    x = torch.from_numpy(rng.standard_normal((T, H)).astype(np.float32)).to(torch.bfloat16)
+    bits = x.view(torch.int16).numpy().view(np.uint16)
+    idx, w = orc.route(logits, k, renormalize=True)
+    lay = orc.layout(idx, E, R)
+    pl, sc = orc.payload(bits, lay["row_slot"], k, 3)
+    q, s = orc.quantize_rows(bits, int4=True)
+    tok = lay["row_slot"] // k
+    assert pl.shape == (lay["N"], H // 2)
+    np.testing.assert_array_equal(pl, q[tok])
+    np.testing.assert_array_equal(sc, s[tok])
+    y = orc.combine(pl, sc, lay["slot_row"], w, T, k, int4=True)
+    yf = torch.from_numpy(y.view(np.int16)).view(torch.bfloat16).float().numpy()
+    xf = x.float().numpy()
+    assert np.all(np.abs(yf - xf) <= (s[:, None] / 2 + np.abs(xf) * 2.0 ** -7) * 1.001)
