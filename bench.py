@@ -38,24 +38,26 @@ FALLBACK_HBM_GBS = 6400.0
 L2_BYTES = 126 * 1024 * 1024
 METRIC = "dispatch+combine tokens/s and HBM GB/s as % of B300 peak (T=16384,H=4096)"
 TRAFFIC_FILE = ROOT / "profiles" / "roofline_traffic.json"
-PAYLOAD_MODE = {"bf16": 0, "int8": 1, "fp8": 2}
+PAYLOAD_MODE = {"bf16": 0, "int8": 1, "fp8": 2, "int4": 3}
+PAYLOAD_BYTES = {"bf16": 2.0, "int8": 1.0, "fp8": 1.0, "int4": 0.5}  # per element
 
 
 # ----------------------------------------------------------------------------
 # algorithmic bytes (per step, per kernel)
 # ----------------------------------------------------------------------------
-def algorithmic_bytes(T, H, E, k, N, payload_int8, out_int8=False):
+def algorithmic_bytes(T, H, E, k, N, payload_int8, out_int8=False, payload_bytes=None):
     """Bytes each stage must move at least once, with N dispatched rows.
 
     route:    logits T*E*4 read
-    dispatch: x T*H*2 read; payload N*H*b written (+ scales N*4 for int8 / FP8 codes)
-    combine:  expert outputs N*H*b_out read (+ N*4 scales if int8); y T*H*2 written
+    dispatch: x T*H*2 read; payload N*H*b written (+ scales N*4 for int8 / FP8 / int4 codes)
+    combine:  expert outputs N*H*b_out read (+ N*4 scales if coded); y T*H*2 written
     Routing metadata (indices, weights, slot maps: ~16*T*k bytes) is kept apart.
+    b = payload_bytes per element when given (0.5 for int4), else 1 or 2.
     """
-    b = 1 if payload_int8 else 2
+    b = payload_bytes if payload_bytes is not None else (1 if payload_int8 else 2)
     b_out = 1 if out_int8 else 2
     route = T * E * 4
-    dispatch = T * H * 2 + N * H * b + (N * 4 if payload_int8 else 0)
+    dispatch = T * H * 2 + int(N * H * b) + (N * 4 if payload_int8 else 0)
     combine = N * H * b_out + (N * 4 if out_int8 else 0) + T * H * 2
     meta = T * k * 4 * 4
     return dict(route=route, dispatch=dispatch, combine=combine, total=route + dispatch + combine, metadata=meta)
@@ -265,7 +267,8 @@ def cpu_model():
 
 def workload_config(w, payload, n_rows, eager=False, path="fused"):
     rows = n_rows if n_rows is not None else w.max_rows()
-    step_bytes = algorithmic_bytes(w.T, w.H, w.E, w.k, rows, payload != "bf16")["total"]
+    step_bytes = algorithmic_bytes(w.T, w.H, w.E, w.k, rows, payload != "bf16",
+                                   payload_bytes=PAYLOAD_BYTES[payload])["total"]
     l2 = (f"no flush: each step moves {step_bytes / 1e9:.2f} GB, beyond the 126 MB L2" if step_bytes > L2_BYTES else
           f"not flushed: the {step_bytes / 1e6:.1f} MB step fits in the 126 MB L2 (latency-bound shape)")
     return {"workload": w.name, "T": w.T, "H": w.H, "E": w.E, "k": w.k, "R": w.R,
@@ -391,7 +394,7 @@ def run_gpu(args):
     tokens = w.T * args.steps * world
     value = tokens / total_s
 
-    nb = algorithmic_bytes(w.T, w.H, w.E, w.k, N, p8 != 0)
+    nb = algorithmic_bytes(w.T, w.H, w.E, w.k, N, p8 != 0, payload_bytes=PAYLOAD_BYTES[args.payload])
     nb["route+dispatch"] = nb["route"] + nb["dispatch"]
     peak, peak_src = measured_peak_gbs()
     step_gbs = nb["total"] / (ms_per_step / 1e3) / 1e9
@@ -602,7 +605,7 @@ def parse_args(argv=None):
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="capacity")
-    ap.add_argument("--payload", choices=["int8", "bf16", "fp8"], default=None)
+    ap.add_argument("--payload", choices=["int8", "bf16", "fp8", "int4"], default=None)
     ap.add_argument("--path", choices=["calls", "fused"], default="fused",
                     help="fused: ep_route_dispatch + ep_combine; calls: ep_route, ep_dispatch, ep_combine")
     ap.add_argument("--pipeline", default=None,

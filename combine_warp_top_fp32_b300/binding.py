@@ -27,13 +27,14 @@ EP_ERR_DEVICE_INDEX = 5
 EP_PAYLOAD_BF16 = 0
 EP_PAYLOAD_INT8 = 1
 EP_PAYLOAD_FP8 = 2  # FP8 E4M3 codes (bytes) + one fp32 scale per row
+EP_PAYLOAD_INT4 = 3  # 4-bit codes, two per byte ([rows, H/2] bytes) + one fp32 scale per row
 
 # Every symbol include/ep.h declares.
 EXPORTS = (
     "ep_status_string", "ep_config_check", "ep_capacity", "ep_max_rows", "ep_workspace_size",
     "ep_workspace_init", "ep_route", "ep_dispatch", "ep_combine", "ep_quantize_rows", "ep_get_error",
     "ep_load_stats", "ep_dispatch_static", "ep_route_dispatch", "ep_quantize_rows_fp8", "ep_bitmap_encode",
-    "ep_bitmap_layout",
+    "ep_bitmap_layout", "ep_quantize_rows_int4",
 )
 
 
@@ -78,6 +79,7 @@ def _load():
     lib.ep_combine.argtypes = [CFG, P, P, I32, P, P, P, P, SZ, P]
     lib.ep_quantize_rows.argtypes = [P, I64, I32, P, P, P]
     lib.ep_quantize_rows_fp8.argtypes = [P, I64, I32, P, P, P]
+    lib.ep_quantize_rows_int4.argtypes = [P, I64, I32, P, P, P]
     lib.ep_bitmap_encode.argtypes = [CFG, P, P, P, SZ, P]
     lib.ep_bitmap_layout.argtypes = [CFG, P, P, P, P, P, P, P, P, SZ, P]
     lib.ep_get_error.argtypes = [P, SZ, P]
@@ -117,14 +119,17 @@ def config_from_workload(w, payload=None, renormalize=None) -> ep_config_t:
 _PAYLOAD_DTYPES = (torch.bfloat16, torch.int8, torch.uint8, torch.float8_e4m3fn)
 
 
-def payload_kind(t: torch.Tensor) -> int:
-    """EP_PAYLOAD_* of a payload / expert-output tensor from its dtype."""
+def payload_kind(t: torch.Tensor, H: int | None = None) -> int:
+    """EP_PAYLOAD_* of a payload / expert-output tensor from its dtype (and,
+    for bytes, its width: H/2 columns are packed int4, H columns E4M3)."""
     if t.dtype == torch.bfloat16:
         return EP_PAYLOAD_BF16
     if t.dtype == torch.int8:
         return EP_PAYLOAD_INT8
-    if t.dtype in (torch.uint8, torch.float8_e4m3fn):
+    if t.dtype == torch.float8_e4m3fn:
         return EP_PAYLOAD_FP8
+    if t.dtype == torch.uint8:
+        return EP_PAYLOAD_INT4 if H is not None and t.shape[-1] * 2 == H else EP_PAYLOAD_FP8
     raise ValueError(f"unsupported payload dtype {t.dtype}")
 
 
@@ -260,6 +265,12 @@ def ep_bitmap_layout(cfg, bitmap, row_token, expert_counts, expert_raw, expert_o
                                 ws.numel() * ws.element_size(), _stream(stream)), "ep_bitmap_layout")
 
 
+def ep_quantize_rows_int4(inp, q, scales, stream=None):
+    n, H = inp.shape
+    _check(lib.ep_quantize_rows_int4(_ptr(inp, torch.bfloat16, "in"), int(n), int(H), _ptr(q, torch.uint8, "q"),
+                                     _ptr(scales, torch.float32, "scales"), _stream(stream)), "ep_quantize_rows_int4")
+
+
 def ep_get_error(ws, stream=None) -> int:
     """Synchronise the stream and return (and clear) the device status code."""
     return lib.ep_get_error(_ptr(ws, what="ws"), ws.numel() * ws.element_size(), _stream(stream))
@@ -288,13 +299,15 @@ class EpBuffers:
         T, H, E, k, R = cfg.T, cfg.H, cfg.E, cfg.k, cfg.R
         rows = ep_max_rows(cfg)
         coded = cfg.payload != EP_PAYLOAD_BF16
-        pdtype = {EP_PAYLOAD_BF16: torch.bfloat16, EP_PAYLOAD_INT8: torch.int8, EP_PAYLOAD_FP8: torch.uint8}[cfg.payload]
+        pdtype = {EP_PAYLOAD_BF16: torch.bfloat16, EP_PAYLOAD_INT8: torch.int8, EP_PAYLOAD_FP8: torch.uint8,
+                  EP_PAYLOAD_INT4: torch.uint8}[cfg.payload]
+        pcols = H // 2 if cfg.payload == EP_PAYLOAD_INT4 else H
         i32 = dict(dtype=torch.int32, device=device)
         b = EpBuffers(
             cfg=cfg,
             topk_idx=torch.empty((T, k), **i32),
             topk_w=torch.empty((T, k), dtype=torch.float32, device=device),
-            payload=torch.empty((rows, H), dtype=pdtype, device=device),
+            payload=torch.empty((rows, pcols), dtype=pdtype, device=device),
             scales=torch.empty((rows,), dtype=torch.float32, device=device) if coded else None,
             row_slot=torch.empty((rows,), **i32),
             slot_row=torch.empty((T * k,), **i32),
@@ -324,7 +337,7 @@ class EpBuffers:
                           self.n_dropped, self.ws, stream)
 
     def combine(self, expert_out, out_scales=None, stream=None):
-        out_payload = payload_kind(expert_out)
+        out_payload = payload_kind(expert_out, self.cfg.H)
         ep_combine(self.cfg, expert_out, out_scales, out_payload, self.slot_row, self.topk_w, self.y, self.ws, stream)
 
     def step(self, logits, x, expert_out, out_scales=None, stream=None):

@@ -30,10 +30,10 @@ namespace {
 
 constexpr unsigned kFull = 0xffffffffu;
 
-// Elements of one 16-byte chunk: 8 bf16, or 16 int8 / E4M3 codes.
+// Elements of one 16-byte chunk: 8 bf16, 16 int8 / E4M3 codes or 32 int4 codes.
 template <int FMT>
 struct Chunk {
-  static constexpr int kElems = FMT == kFmtBf16 ? 8 : 16;
+  static constexpr int kElems = FMT == kFmtBf16 ? 8 : (FMT == kFmtInt4 ? 32 : 16);
 };
 
 // acc[0..EL) += w * v for one 16-byte chunk of a kept row, in element order;
@@ -47,6 +47,12 @@ __device__ __forceinline__ void fma_chunk(float* acc, uint4 v, float w, float sc
     for (int q = 0; q < 4; ++q)
 #pragma unroll
       for (int i = 0; i < 4; ++i) acc[4 * q + i] = __fmaf_rn(w, __fmul_rn(i8_at(u[q], i), sc), acc[4 * q + i]);
+  } else if constexpr (FMT == kFmtInt4) {
+    const uint32_t u[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+#pragma unroll
+      for (int i = 0; i < 8; ++i) acc[8 * q + i] = __fmaf_rn(w, __fmul_rn(i4_at(u[q], i), sc), acc[8 * q + i]);
   } else if constexpr (FMT == kFmtFp8) {
     const uint32_t u[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
@@ -142,7 +148,7 @@ __global__ void __launch_bounds__(256, 2) combine_kernel(const CombineArgs a) {
   const int64_t warp0 = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
   const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
   const int nchunk = a.H / EL;
-  const int64_t row_bytes = kCoded ? a.H : 2 * static_cast<int64_t>(a.H);
+  const int64_t row_bytes = static_cast<int64_t>(a.H) * (FMT == kFmtBf16 ? 2 : 1) / (FMT == kFmtInt4 ? 2 : 1);
   const char* base = static_cast<const char*>(a.expert_out);
   pdl_wait();  // slot rows, weights and expert outputs come from earlier kernels
   pdl_launch_dependents();
@@ -222,7 +228,8 @@ __global__ void __launch_bounds__(256, 2) combine_kernel(const CombineArgs a) {
 }
 
 // One row per CTA iteration; 16 elements per thread; the same code as the
-// dispatch (int8: scale = amax/127; FP8 E4M3: scale = amax/448).
+// dispatch (int8: scale = amax/127; FP8 E4M3: amax/448; int4: amax/7, rows of
+// H/2 bytes).
 template <int FMT>
 __global__ void __launch_bounds__(1024) quantize_rows_kernel(const void* __restrict__ in, int64_t n, int H,
                                                               uint8_t* __restrict__ q, float* __restrict__ scales) {
@@ -247,7 +254,11 @@ __global__ void __launch_bounds__(1024) quantize_rows_kernel(const void* __restr
     float am = amax_s[buf][0];
     for (int i = 1; i < nw; ++i) am = fmaxf(am, amax_s[buf][i]);
     const float scale = __fdiv_rn(am, CodeMax<FMT>::kValue);
-    if (on) st_v4(q + t * H + 16 * c, quant16_fmt<FMT>(a0, a1, scale, __frcp_rn(scale)));
+    if constexpr (FMT == kFmtInt4) {
+      if (on) st_v2(q + t * (H / 2) + 8 * c, quant16_int4_coded(a0, a1, scale, __frcp_rn(scale)));
+    } else {
+      if (on) st_v4(q + t * H + 16 * c, quant16_fmt<FMT>(a0, a1, scale, __frcp_rn(scale)));
+    }
     if (c == 0) scales[t] = scale;
     buf ^= 1;
   }
@@ -257,7 +268,7 @@ __global__ void __launch_bounds__(1024) quantize_rows_kernel(const void* __restr
 
 namespace {
 
-int g_occ_combine[6][64];
+int g_occ_combine[8][64];
 
 template <int FMT, int LOADS>
 cudaError_t launch_combine_t(CombineArgs a, int sms, int* cache, cudaStream_t s) {
@@ -281,7 +292,8 @@ cudaError_t launch_combine_t(CombineArgs a, int sms, int* cache, cudaStream_t s)
 template <int FMT>
 cudaError_t launch_combine_fmt(const CombineArgs& a, int sms, cudaStream_t s) {
   // 16 loads in flight per lane once a row is long enough to keep them busy
-  const bool deep = a.H / Chunk<FMT>::kElems >= 64;
+  // (8 for int4, whose 32-element chunks need twice the accumulators)
+  const bool deep = FMT != kFmtInt4 && a.H / Chunk<FMT>::kElems >= 64;
   return deep ? launch_combine_t<FMT, 16>(a, sms, g_occ_combine[2 * FMT], s)
               : launch_combine_t<FMT, 8>(a, sms, g_occ_combine[2 * FMT + 1], s);
 }
@@ -290,6 +302,7 @@ cudaError_t launch_combine_fmt(const CombineArgs& a, int sms, cudaStream_t s) {
 
 cudaError_t launch_combine(const CombineArgs& a, int sms, cudaStream_t s) {
   if (a.T == 0) return cudaSuccess;
+  if (a.out_fmt == kFmtInt4) return launch_combine_fmt<kFmtInt4>(a, sms, s);
   if (a.out_fmt == kFmtFp8) return launch_combine_fmt<kFmtFp8>(a, sms, s);
   if (a.out_fmt == kFmtInt8) return launch_combine_fmt<kFmtInt8>(a, sms, s);
   return launch_combine_fmt<kFmtBf16>(a, sms, s);
@@ -299,13 +312,14 @@ cudaError_t launch_quantize_rows(const void* in, int64_t n, int H, int fmt, void
                                  cudaStream_t s) {
   if (n == 0) return cudaSuccess;
   const int block = ((H / 16 + 31) / 32) * 32;
-  static int occ[2][32][64];  // per format, block size / 32 and device
+  static int occ[3][32][64];  // per format, block size / 32 and device
   auto go = [&](auto kernel, int which) {
     const int per_sm = resident_ctas(kernel, block, 0, occ[which][block / 32 - 1]);
     const int64_t want = static_cast<int64_t>(sms) * per_sm;
     const int grid = static_cast<int>(n < want ? n : want);
     return launch_pdl(kernel, grid, block, 0, s, in, n, H, static_cast<uint8_t*>(q), scales);
   };
+  if (fmt == kFmtInt4) return go(quantize_rows_kernel<kFmtInt4>, 2);
   return fmt == kFmtFp8 ? go(quantize_rows_kernel<kFmtFp8>, 1) : go(quantize_rows_kernel<kFmtInt8>, 0);
 }
 

@@ -268,13 +268,14 @@ __device__ __forceinline__ void ld_x32(const char* p, uint4& lo, uint4& hi) {
   }
 }
 
-// int8 or FP8 payload: one CTA per token in flight (grid-stride). Thread c codes the
+// int8, FP8 or int4 payload: one CTA per token in flight (grid-stride). Thread c codes the
 // 16-element groups c and c + blockDim.x of the row, so that every warp-wide
 // store covers whole 32-byte sectors. The next token's row is loaded while
 // this one is coded; threads j < k carry slot j's row (rows pipeline above,
 // two tokens ahead). amax: exact per-thread halfword maxima, a warp max and one
-// shared-memory step; scale = amax/127 (int8) or amax/448 (FP8) with IEEE
-// division; the code is the branch-free corrected-quotient path.
+// shared-memory step; scale = amax/127 (int8), amax/448 (FP8) or amax/7
+// (int4) with IEEE division; the code is the branch-free corrected-quotient
+// path; an int4 group is 8 bytes of packed nibbles.
 template <bool V8, int FMT>
 __global__ void __launch_bounds__(512) scatter_code_kernel(const DispatchArgs a, int tile_log2) {
   constexpr int G = 2;  // 16-element groups per thread
@@ -342,10 +343,18 @@ __global__ void __launch_bounds__(512) scatter_code_kernel(const DispatchArgs a,
     for (int g = 0; g < G; ++g) {
       const int grp = c + g * B;
       if (grp >= ngroup) break;
-      const uint4 q = quant16_fmt<FMT>(cur[2 * g], cur[2 * g + 1], scale, inv);
-      for (int j = 0; j < a.k; ++j) {
-        const int row = rows_s[buf][j];
-        if (row >= 0) st_v4(static_cast<int8_t*>(a.payload) + static_cast<int64_t>(row) * a.H + 16 * grp, q);
+      if constexpr (FMT == kFmtInt4) {  // 8 bytes of packed nibbles per group, rows of H/2 bytes
+        const uint2 q = quant16_int4_coded(cur[2 * g], cur[2 * g + 1], scale, inv);
+        for (int j = 0; j < a.k; ++j) {
+          const int row = rows_s[buf][j];
+          if (row >= 0) st_v2(static_cast<char*>(a.payload) + static_cast<int64_t>(row) * (a.H / 2) + 8 * grp, q);
+        }
+      } else {
+        const uint4 q = quant16_fmt<FMT>(cur[2 * g], cur[2 * g + 1], scale, inv);
+        for (int j = 0; j < a.k; ++j) {
+          const int row = rows_s[buf][j];
+          if (row >= 0) st_v4(static_cast<int8_t*>(a.payload) + static_cast<int64_t>(row) * a.H + 16 * grp, q);
+        }
       }
     }
     if (slot && my_row >= 0) a.scales[my_row] = scale;
@@ -491,14 +500,16 @@ cudaError_t launch_scan_scatter(const DispatchArgs& a, int sms, cudaStream_t s) 
     // up to whole warps (>= 32 >= k)
     const int block = (((a.H / 16 + 1) / 2 + 31) / 32) * 32;
     const bool v8 = (reinterpret_cast<uintptr_t>(a.x) & 31u) == 0;  // rows are then 32-byte aligned too
-    static int occ[4][16][64];  // per load width x format, block size / 32, device
+    static int occ[6][16][64];  // per load width x format, block size / 32, device
     auto go = [&](auto kernel, int which) {
       const int per_sm = resident_ctas(kernel, block, 0, occ[which][block / 32 - 1]);
       const int64_t want = static_cast<int64_t>(sms) * per_sm;
       const int grid = static_cast<int>(a.T < want ? a.T : want);
       return launch_pdl(kernel, grid, block, 0, s, a, tile_log2);
     };
-    if (a.fmt == kFmtFp8)
+    if (a.fmt == kFmtInt4)
+      err = v8 ? go(scatter_code_kernel<true, kFmtInt4>, 5) : go(scatter_code_kernel<false, kFmtInt4>, 4);
+    else if (a.fmt == kFmtFp8)
       err = v8 ? go(scatter_code_kernel<true, kFmtFp8>, 3) : go(scatter_code_kernel<false, kFmtFp8>, 2);
     else
       err = v8 ? go(scatter_code_kernel<true, kFmtInt8>, 1) : go(scatter_code_kernel<false, kFmtInt8>, 0);

@@ -41,8 +41,8 @@ bool config_ok(const ep_config_t* c) {
   if (c->R < 1 || c->E % c->R != 0) return false;
   if (isnan(c->capacity_factor) || isinf(c->capacity_factor)) return false;
   if (c->renormalize != 0 && c->renormalize != 1) return false;
-  if (c->payload != EP_PAYLOAD_BF16 && c->payload != EP_PAYLOAD_INT8 && c->payload != EP_PAYLOAD_FP8_E4M3)
-    return false;
+  if (c->payload < EP_PAYLOAD_BF16 || c->payload > EP_PAYLOAD_INT4) return false;
+  if (c->payload == EP_PAYLOAD_INT4 && c->H % 32 != 0) return false;  // rows of H/2 bytes, 16-byte aligned
   if (static_cast<int64_t>(c->T) * c->k > INT32_MAX) return false;
   return true;
 }
@@ -146,6 +146,7 @@ ep_status_t carve_layout(const ep_config_t* cfg, int32_t* expert_counts, int32_t
 ep_status_t quantize_rows(const void* in, int64_t n, int32_t H, int fmt, void* q, float* scales,
                           cudaStream_t stream) {
   if (n < 0 || H < 16 || H > kMaxH || H % 16 != 0) return EP_ERR_INVALID_ARG;
+  if (fmt == ep::kFmtInt4 && H % 32 != 0) return EP_ERR_INVALID_ARG;
   if (n == 0) return EP_OK;
   if (!in || !q || !scales || !aligned(in, 16) || !aligned(q, 16) || !aligned(scales, 4)) return EP_ERR_INVALID_ARG;
   const int sms = current_sm_count();
@@ -278,8 +279,8 @@ ep_status_t ep_combine(const ep_config_t* cfg, const void* expert_out, const flo
                        int32_t out_payload, const int32_t* slot_row, const float* topk_w, void* y, void* ws,
                        size_t ws_bytes, cudaStream_t stream) {
   if (!config_ok(cfg)) return EP_ERR_INVALID_ARG;
-  if (out_payload != EP_PAYLOAD_BF16 && out_payload != EP_PAYLOAD_INT8 && out_payload != EP_PAYLOAD_FP8_E4M3)
-    return EP_ERR_INVALID_ARG;
+  if (out_payload < EP_PAYLOAD_BF16 || out_payload > EP_PAYLOAD_INT4) return EP_ERR_INVALID_ARG;
+  if (out_payload == EP_PAYLOAD_INT4 && cfg->H % 32 != 0) return EP_ERR_INVALID_ARG;
   if (ws == nullptr || ws_bytes < 256 || !aligned(ws, 256)) return EP_ERR_WORKSPACE;
   if (cfg->T == 0) return EP_OK;
   const bool coded = out_payload != EP_PAYLOAD_BF16;
@@ -311,6 +312,11 @@ ep_status_t ep_quantize_rows(const void* in, int64_t n, int32_t H, int8_t* q, fl
 ep_status_t ep_quantize_rows_fp8(const void* in, int64_t n, int32_t H, uint8_t* q, float* scales,
                                  cudaStream_t stream) {
   return quantize_rows(in, n, H, ep::kFmtFp8, q, scales, stream);
+}
+
+ep_status_t ep_quantize_rows_int4(const void* in, int64_t n, int32_t H, uint8_t* q, float* scales,
+                                  cudaStream_t stream) {
+  return quantize_rows(in, n, H, ep::kFmtInt4, q, scales, stream);
 }
 
 ep_status_t ep_get_error(void* ws, size_t ws_bytes, cudaStream_t stream) {

@@ -226,8 +226,68 @@ __device__ __forceinline__ uint4 quant16_fp8_coded(uint4 a0, uint4 a1, float sca
   return quant16_fp8_ieee(a0, a1, scale);
 }
 
+// ---- per-token 4-bit code of 16 consecutive elements -------------------------
+// scale = amax / 7; q = clamp(rint(x / scale), -7, 7), two's-complement
+// nibbles, the lower-indexed element in the low nibble: 16 elements -> 8
+// bytes. The corrected quotient rounds like the IEEE quotient for every bf16
+// amax with amax/7 >= 2^-100 and bf16 |x| <= amax (checked exhaustively on
+// the host, 525,448,784 pairs), and |q| <= 7 there, so no clamp is needed.
+
+// Low nibbles of four words (q mod 16 in bits 0-3 of each) -> 16 bits.
+__device__ __forceinline__ uint32_t pack4_nibbles(uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+  uint32_t x = pack4_low_bytes(a, b, c, d) & 0x0F0F0F0Fu;  // nibble i in byte i
+  x = (x | (x >> 4)) & 0x00FF00FFu;                          // pairs in bytes 0 and 2
+  return (x | (x >> 8)) & 0xFFFFu;
+}
+
+__device__ __forceinline__ uint2 quant16_int4_fast(uint4 a0, uint4 a1, float scale, float inv) {
+  const uint64_t inv2 = f32x2_pack(__float_as_uint(inv), __float_as_uint(inv));
+  const uint64_t nsc2 = f32x2_pack(__float_as_uint(-scale), __float_as_uint(-scale));
+  const uint64_t mg2 = f32x2_pack(0x4B400000u, 0x4B400000u);  // 1.5 * 2^23 in both halves
+  const uint32_t w[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+  uint32_t tb[16];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const uint64_t x2 = f32x2_pack(w[i] << 16, w[i] & 0xffff0000u);
+    const uint64_t q0 = f32x2_mul(x2, inv2);
+    const uint64_t t = f32x2_add(f32x2_fma(f32x2_fma(q0, nsc2, x2), inv2, q0), mg2);
+    tb[2 * i] = static_cast<uint32_t>(t);
+    tb[2 * i + 1] = static_cast<uint32_t>(t >> 32);
+  }
+  return make_uint2(pack4_nibbles(tb[0], tb[1], tb[2], tb[3]) | (pack4_nibbles(tb[4], tb[5], tb[6], tb[7]) << 16),
+                    pack4_nibbles(tb[8], tb[9], tb[10], tb[11]) | (pack4_nibbles(tb[12], tb[13], tb[14], tb[15]) << 16));
+}
+
+__device__ __forceinline__ uint2 quant16_int4_ieee(uint4 a0, uint4 a1, float scale) {
+  const uint32_t w[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+  uint32_t q[16];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const float v = h ? bf16_hi(w[i]) : bf16_lo(w[i]);
+      int r = (scale == 0.0f) ? 0 : __float2int_rn(__fdiv_rn(v, scale));
+      r = max(-7, min(7, r));
+      q[2 * i + h] = static_cast<uint32_t>(r);
+    }
+  }
+  return make_uint2(pack4_nibbles(q[0], q[1], q[2], q[3]) | (pack4_nibbles(q[4], q[5], q[6], q[7]) << 16),
+                    pack4_nibbles(q[8], q[9], q[10], q[11]) | (pack4_nibbles(q[12], q[13], q[14], q[15]) << 16));
+}
+
+__device__ __forceinline__ uint2 quant16_int4_coded(uint4 a0, uint4 a1, float scale, float inv) {
+  if (scale >= kFastScaleMin) return quant16_int4_fast(a0, a1, scale, inv);
+  return quant16_int4_ieee(a0, a1, scale);
+}
+
+// Nibble i of a word (two's complement) as an exact float: 2^23 + (q ^ 8),
+// built from the bits, minus 2^23 + 8.
+__device__ __forceinline__ float i4_at(uint32_t w, int i) {
+  return __fsub_rn(__uint_as_float(0x4B000000u | (((w >> (4 * i)) & 0xFu) ^ 0x8u)), 8388616.0f);
+}
+
 // Payload formats of the row codes.
-enum PayloadFmt : int { kFmtBf16 = 0, kFmtInt8 = 1, kFmtFp8 = 2 };
+enum PayloadFmt : int { kFmtBf16 = 0, kFmtInt8 = 1, kFmtFp8 = 2, kFmtInt4 = 3 };
 
 // Largest code magnitude: the scale is amax / kCodeMax.
 template <int FMT>
@@ -239,6 +299,10 @@ struct CodeMax<kFmtInt8> {
 template <>
 struct CodeMax<kFmtFp8> {
   static constexpr float kValue = 448.0f;
+};
+template <>
+struct CodeMax<kFmtInt4> {
+  static constexpr float kValue = 7.0f;
 };
 
 template <int FMT>

@@ -62,14 +62,17 @@ typedef enum {
 typedef enum {
   EP_PAYLOAD_BF16 = 0,     /* rows are the token's bf16 bytes, unchanged                   */
   EP_PAYLOAD_INT8 = 1,     /* rows are the token's int8 code + one fp32 scale per row      */
-  EP_PAYLOAD_FP8_E4M3 = 2  /* rows are the token's FP8 E4M3 code + one fp32 scale per row  */
+  EP_PAYLOAD_FP8_E4M3 = 2, /* rows are the token's FP8 E4M3 code + one fp32 scale per row  */
+  EP_PAYLOAD_INT4 = 3      /* rows of H/2 bytes: the token's 4-bit code, two per byte, + one
+                              fp32 scale per row (H % 32 == 0)                              */
 } ep_payload_t;
 
 /*
  * Problem statement (ThunderEP §1.3: T tokens, hidden size, E experts, top-k,
  * N cards; juhe.plus all-to-all volume 2*T*k*H*b).
  *   T                tokens in the batch, >= 0
- *   H                hidden size, 16 <= H <= 16384, H % 16 == 0
+ *   H                hidden size, 16 <= H <= 16384, H % 16 == 0 (H % 32 == 0
+ *                    with the int4 payload)
  *   E                experts, 1 <= E <= 1024
  *   k                experts per token, 1 <= k <= min(E, 32)
  *   R                virtual ranks, R >= 1, E % R == 0
@@ -88,6 +91,9 @@ typedef enum {
  *   int8  scale = amax/127.0f, q = clamp(rint(x/scale), -127, 127)
  *   FP8   scale = amax/448.0f, q = E4M3 round-to-nearest-even of x/scale,
  *         saturated to +-448 (OCP E4M3: bias 7, 3 mantissa bits, no inf)
+ *   int4  scale = amax/7.0f, q = clamp(rint(x/scale), -7, 7) as a
+ *         two's-complement nibble; byte i of a row holds elements 2i (low
+ *         nibble) and 2i+1 (high nibble)
  * with IEEE fp32 division and amax = 0 giving scale 0 and all-zero codes.
  */
 typedef struct {
@@ -141,7 +147,9 @@ ep_status_t ep_route(const ep_config_t* cfg, const float* logits, int32_t* topk_
  *   topk_idx       [T, k] int32 in    k distinct expert ids per token
  *   payload        [max_rows, H] out  bf16 (EP_PAYLOAD_BF16), int8
  *                                     (EP_PAYLOAD_INT8) or E4M3 bytes
- *                                     (EP_PAYLOAD_FP8_E4M3); rows [0, N) are
+ *                                     (EP_PAYLOAD_FP8_E4M3), or [max_rows,
+ *                                     H/2] packed int4 (EP_PAYLOAD_INT4);
+ *                                     rows [0, N) are
  *                                     written, N = T*k - dropped; row order is
  *                                     (expert, token), so rank r's block is
  *                                     rows [rank_off[r], rank_off[r+1])
@@ -252,16 +260,20 @@ ep_status_t ep_dispatch_static(const ep_config_t* cfg, const void* x, const int3
  * ep_combine — weighted top-k recombination (ThunderEP §1.3 steps 3-4).
  *   expert_out   [max_rows, H] in  bf16 (out_payload = EP_PAYLOAD_BF16), int8
  *                                  (EP_PAYLOAD_INT8) or E4M3 bytes
- *                                  (EP_PAYLOAD_FP8_E4M3) expert outputs,
- *                                  row-aligned with the dispatch payload
- *   out_scales   [max_rows] fp32   per-row scales for int8 / FP8 rows, else NULL
+ *                                  (EP_PAYLOAD_FP8_E4M3), or [max_rows, H/2]
+ *                                  packed int4 (EP_PAYLOAD_INT4) expert
+ *                                  outputs, row-aligned with the dispatch
+ *                                  payload
+ *   out_scales   [max_rows] fp32   per-row scales for int8 / FP8 / int4 rows,
+ *                                  else NULL
  *   slot_row     [T*k] int32 in    from ep_dispatch (-1 = dropped slot)
  *   topk_w       [T, k] fp32 in    from ep_route
  *   y            [T, H] bf16 out   y[t] = bf16_rne(sum over j = 0..k-1 in
  *                                  order, slot not dropped, of
  *                                  fmaf(w[t,j], v_j, acc)), acc starting at 0,
  *                                  v_j = float(bf16) or (float)q * scale
- *                                  (q the int8 or E4M3 code, widened exactly)
+ *                                  (q the int8, E4M3 or int4 code, widened
+ *                                  exactly)
  *   ws, ws_bytes workspace (its status word records bad slot_row entries)
  * A token whose k slots were all dropped gets y = 0.
  */
@@ -285,6 +297,14 @@ ep_status_t ep_quantize_rows(const void* in, int64_t n, int32_t H, int8_t* q, fl
  */
 ep_status_t ep_quantize_rows_fp8(const void* in, int64_t n, int32_t H, uint8_t* q, float* scales,
                                  cudaStream_t stream);
+
+/*
+ * ep_quantize_rows_int4 — the per-token 4-bit code (scale = amax/7) of n rows,
+ * for an expert side that returns 4-bit outputs: q [n, H/2] packed nibbles
+ * out (16-byte aligned), H % 32 == 0; as ep_quantize_rows otherwise.
+ */
+ep_status_t ep_quantize_rows_int4(const void* in, int64_t n, int32_t H, uint8_t* q, float* scales,
+                                  cudaStream_t stream);
 
 /*
  * ep_get_error — synchronises `stream`, reads the workspace's status word,

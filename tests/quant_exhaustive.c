@@ -1,14 +1,16 @@
 /*
  * Host-side proof of the division-free per-token codes of the CUDA kernels
- * (quant16_fast for int8, quant16_fp8_fast for FP8 E4M3): for every bf16
- * amax whose scale = amax/D (IEEE fp32 division; D = 127 for int8, 448 for
- * E4M3) is at least 2^-100, and every bf16 x with |x| <= amax, the corrected
+ * (quant16_fast for int8, quant16_fp8_fast for FP8 E4M3, quant16_int4_fast
+ * for int4): for every bf16 amax whose scale = amax/D (IEEE fp32 division;
+ * D = 127 for int8, 448 for E4M3, 7 for int4) is at least 2^-100, and every
+ * bf16 x with |x| <= amax, the corrected
  * quotient
  *     q0 = fl(x * inv), inv = fl(1/scale)
  *     rem = fma(-q0, scale, x), q1 = fma(rem, inv, q0)
  * gives the same code as the IEEE quotient fl(x / scale):
- *   int8: rint(q1) (ties to even, by adding 1.5 * 2^23) equals rint(fl(x/s));
- *         negative x follow by symmetry (every step rounds to nearest-even);
+ *   int8, int4: rint(q1) (ties to even, by adding 1.5 * 2^23) equals
+ *         rint(fl(x/s)) clamped to D (and never exceeds D itself); negative x
+ *         follow by symmetry (every step rounds to nearest-even);
  *   E4M3: with x's sign put on q1, the nearest-even E4M3 code of q1 (all 8
  *         bits, saturated to 448) equals that of fl(x/s), for both signs of
  *         x (so -0 codes as 0x80 on both sides).
@@ -55,29 +57,40 @@ static float with_sign_of(float q, float x) { return copysignf(fabsf(q), x); }
 
 int main(void) {
   const float magic = 12582912.0f; /* 1.5 * 2^23 */
-  long long pairs = 0, bad = 0, bad_plain = 0, pairs8 = 0, bad8 = 0, bad8_plain = 0;
-#pragma omp parallel for schedule(dynamic, 64) reduction(+ : pairs, bad, bad_plain, pairs8, bad8, bad8_plain)
+  long long pairs = 0, bad = 0, bad_plain = 0, pairs8 = 0, bad8 = 0, bad8_plain = 0, pairs4 = 0, bad4 = 0,
+            bad4_plain = 0;
+#pragma omp parallel for schedule(dynamic, 64) \
+    reduction(+ : pairs, bad, bad_plain, pairs8, bad8, bad8_plain, pairs4, bad4, bad4_plain)
   for (int a = 1; a <= 0x7F7F; ++a) { /* every positive finite bf16 amax */
     const float amax = bf16_value((uint32_t)a);
-    /* int8: scale = amax / 127 */
-    volatile float s_v = amax / 127.0f;
-    const float s = s_v;
-    if (s >= 0x1p-100f) {
+    /* int8: scale = amax / 127; int4: scale = amax / 7 */
+    for (int d = 0; d < 2; ++d) {
+      const float D = d == 0 ? 127.0f : 7.0f;
+      volatile float s_v = amax / D;
+      const float s = s_v;
+      if (s < 0x1p-100f) continue;
       volatile float inv_v = 1.0f / s;
       const float inv = inv_v;
       for (uint32_t xb = 0; xb <= (uint32_t)a; ++xb) { /* every bf16 0 <= x <= amax */
         const float x = bf16_value(xb);
         volatile float qv = x / s;
         float ref = rintf(qv);
-        if (ref > 127.0f) ref = 127.0f;
+        if (ref > D) ref = D;
         volatile float q0_v = x * inv;
         const float q0 = q0_v;
         const float q1 = fmaf(fmaf(-q0, s, x), inv, q0);
         volatile float t1 = q1 + magic;
         volatile float t0 = q0 + magic;
-        ++pairs;
-        if (t1 - magic != ref) ++bad;
-        if (t0 - magic != ref) ++bad_plain;
+        const float r1 = t1 - magic, r0 = t0 - magic;
+        if (d == 0) {
+          ++pairs;
+          if (r1 != ref) ++bad;
+          if (r0 != ref) ++bad_plain;
+        } else {
+          ++pairs4;
+          if (r1 != ref) ++bad4;  /* no clamp on r1: it must not exceed 7 either */
+          if (r0 != ref) ++bad4_plain;
+        }
       }
     }
     /* E4M3: scale = amax / 448, both signs of x */
@@ -103,5 +116,6 @@ int main(void) {
   }
   printf("pairs %lld corrected_mismatch %lld uncorrected_mismatch %lld\n", pairs, bad, bad_plain);
   printf("fp8_pairs %lld fp8_corrected_mismatch %lld fp8_uncorrected_mismatch %lld\n", pairs8, bad8, bad8_plain);
-  return (bad != 0 || bad8 != 0);
+  printf("int4_pairs %lld int4_corrected_mismatch %lld int4_uncorrected_mismatch %lld\n", pairs4, bad4, bad4_plain);
+  return (bad != 0 || bad8 != 0 || bad4 != 0);
 }

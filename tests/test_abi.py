@@ -120,3 +120,11 @@ def test_load_stats_closed_forms(ep, orc):
     assert s["cv"] == 1.0 and s["min"] == 0 and s["max"] == 2
     c = np.random.default_rng(0).integers(0, 1000, 128).astype(np.int32)
     assert math.isclose(ep.ep_load_stats(c)["cv"], orc.count_cv(c), rel_tol=1e-12)
+
+
+def test_int4_payload_needs_h_multiple_of_32(ep):
+    ok = ep.make_config(64, 32, 8, 2, 2, payload=ep.EP_PAYLOAD_INT4)
+    bad = ep.make_config(64, 48, 8, 2, 2, payload=ep.EP_PAYLOAD_INT4)
+    assert ep.ep_config_check(ok) == ep.EP_OK
+    assert ep.ep_config_check(bad) == ep.EP_ERR_INVALID_ARG
+    assert ep.ep_config_check(ep.make_config(64, 48, 8, 2, 2, payload=4)) == ep.EP_ERR_INVALID_ARG

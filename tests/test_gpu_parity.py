@@ -109,8 +109,9 @@ def _full_parity(ep, orc, w, payload, renormalize=False, device_gen="cuda"):
 
 
 CASES = [("tiny", 0), ("decode-latency", 1), ("prefill-mid", 0), ("prefill-mid", 1), ("capacity", 1),
-         # FP8 E4M3 per-token payload (the lower-precision extension)
-         ("decode-latency", 2), ("prefill-mid", 2), ("capacity", 2)]
+         # FP8 E4M3 and int4 per-token payloads (the lower-precision extension)
+         ("decode-latency", 2), ("prefill-mid", 2), ("capacity", 2),
+         ("decode-latency", 3), ("prefill-mid", 3), ("capacity", 3)]
 
 
 @pytest.mark.parametrize("name,payload", CASES)
@@ -130,7 +131,7 @@ def test_workload_parity_renormalized(ep, orc, name):
     _full_parity(ep, orc, workloads.WORKLOADS[name], 0, renormalize=True)
 
 
-@pytest.mark.parametrize("payload", [0, 1, 2])
+@pytest.mark.parametrize("payload", [0, 1, 2, 3])
 def test_large_parity_sampled(ep, orc, payload):
     """T=131072, H=8192, E=256, k=8 at full size, in the bench's launch configuration.
     Routing and all layout metadata compared in full; payload rows and combined
@@ -191,6 +192,9 @@ EDGE = [
     (5, 16, 3, 2, 1, 0.0, 2, 0, "FP8 at minimum H"),
     (1000, 64, 8, 2, 2, 0.5, 2, 1, "FP8 with drops and a ragged last tile"),
     (777, 16384, 4, 2, 2, 0.0, 2, 0, "FP8 at maximum H"),
+    (5, 32, 3, 2, 1, 0.0, 3, 0, "int4 at its minimum H"),
+    (1000, 96, 8, 2, 2, 0.5, 3, 1, "int4 with drops and a ragged last tile"),
+    (777, 16384, 4, 2, 2, 0.0, 3, 0, "int4 at maximum H"),
     (1000, 64, 8, 2, 2, 0.0, 1, 0, "ragged last tile"),
     (2500, 48, 6, 3, 3, 0.0, 0, 1, "E not a power of two, two ragged tiles"),
     (777, 16384, 4, 2, 2, 0.0, 1, 0, "maximum H"),
@@ -254,7 +258,7 @@ def test_empty_batch(ep):
     assert ep.ep_get_error(buf.ws) == ep.EP_OK
 
 
-@pytest.mark.parametrize("fmt", ["int8", "fp8"])
+@pytest.mark.parametrize("fmt", ["int8", "fp8", "int4"])
 @pytest.mark.parametrize("shape", ["prefill-mid", "wide"])
 def test_coded_return_path(ep, orc, shape, fmt):
     """Expert outputs coded per row (ep_quantize_rows / ep_quantize_rows_fp8)
@@ -262,24 +266,26 @@ def test_coded_return_path(ep, orc, shape, fmt):
     with drops)."""
     from combine_warp_top_fp32_b300 import workloads
 
-    fp8 = fmt == "fp8"
+    fp8, int4 = fmt == "fp8", fmt == "int4"
     w = workloads.WORKLOADS["prefill-mid"]
     if shape == "wide":
         w = w.replace(T=1500, H=8192, capacity_factor=1.0, seed=9)
-    kind = ep.EP_PAYLOAD_FP8 if fp8 else ep.EP_PAYLOAD_INT8
+    kind = {"int8": ep.EP_PAYLOAD_INT8, "fp8": ep.EP_PAYLOAD_FP8, "int4": ep.EP_PAYLOAD_INT4}[fmt]
     cfg = ep.config_from_workload(w, payload=kind)
     d = workloads.generate(w, device="cuda")
     rows = w.max_rows()
-    q = torch.empty(rows, w.H, dtype=torch.uint8 if fp8 else torch.int8, device="cuda")
+    q = torch.empty(rows, w.H // 2 if int4 else w.H, dtype=torch.int8 if fmt == "int8" else torch.uint8,
+                    device="cuda")
     s = torch.empty(rows, dtype=torch.float32, device="cuda")
-    (ep.ep_quantize_rows_fp8 if fp8 else ep.ep_quantize_rows)(d["expert_out"], q, s)
+    quant = {"int8": ep.ep_quantize_rows, "fp8": ep.ep_quantize_rows_fp8, "int4": ep.ep_quantize_rows_int4}[fmt]
+    quant(d["expert_out"], q, s)
     torch.cuda.synchronize()
-    q_o, s_o = orc.quantize_rows(_bits(d["expert_out"]), fp8=fp8)
+    q_o, s_o = orc.quantize_rows(_bits(d["expert_out"]), fp8=fp8, int4=int4)
     np.testing.assert_array_equal(q.cpu().numpy(), q_o)
     np.testing.assert_array_equal(s.cpu().numpy(), s_o)
     idx, wts = orc.route(d["logits"].cpu().numpy(), w.k)
     lay = orc.layout(idx, w.E, w.R, w.capacity_factor)
-    y_orc = orc.combine(q_o, s_o, lay["slot_row"], wts, w.T, w.k)
+    y_orc = orc.combine(q_o, s_o, lay["slot_row"], wts, w.T, w.k, int4=int4)
     buf = ep.EpBuffers.allocate(cfg)
     y = torch.empty(w.T, w.H, dtype=torch.bfloat16, device="cuda")
     ep.ep_combine(cfg, q, s, kind, torch.from_numpy(lay["slot_row"]).cuda(), torch.from_numpy(wts).cuda(), y,
@@ -288,7 +294,7 @@ def test_coded_return_path(ep, orc, shape, fmt):
     np.testing.assert_array_equal(_bits(y), y_orc)
 
 
-@pytest.mark.parametrize("payload", [0, 1, 2])
+@pytest.mark.parametrize("payload", [0, 1, 2, 3])
 def test_identity_experts_round_trip(ep, payload):
     """combine(dispatch(x)) with identity experts and renormalised weights gives x back."""
     T, H, E, k, R = 2048, 512, 32, 4, 4
@@ -311,7 +317,7 @@ def test_identity_experts_round_trip(ep, payload):
         s_tok = np.zeros(T)
         rs = buf.row_slot.cpu().numpy()
         s_tok[rs // k] = buf.scales.cpu().numpy()
-        if payload == 1:  # int8: half a code step
+        if payload in (1, 3):  # int8, int4: half a code step
             bound = (s_tok / 2)[:, None] * 1.0001
         else:  # E4M3: 2^-4 relative above 2^-6 * scale, 2^-10 * scale below
             bound = np.maximum(np.abs(xf) * 2.0 ** -4, (s_tok * 2.0 ** -10)[:, None]) * 1.0001
