@@ -67,13 +67,7 @@ __global__ void __launch_bounds__(512) count_kernel(const Pairs src, int T, int 
   __syncthreads();
   if (nt == 0) return;
 
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
-  for (int e = warp; e < E; e += nw) {
-    const int c = lane < TW ? __popc(mask[e * TW + lane]) : 0;
-    const int incl = warp_inclusive_scan(c);
-    if (lane < TW) pre[e * TW + lane] = static_cast<uint32_t>(incl - c);
-    if (lane == 31) tile_counts[static_cast<int64_t>(e) * ntiles + b] = incl;
-  }
+  tile_word_prefix(mask, pre, E, TW, tile_counts, ntiles, b);
   __syncthreads();
 
   for (int p = threadIdx.x; p < npairs; p += blockDim.x) {
@@ -87,25 +81,6 @@ __global__ void __launch_bounds__(512) count_kernel(const Pairs src, int T, int 
     }
     lrank[base + p] = r;
   }
-}
-
-// Exclusive scan of one value per thread over a 256-thread block; returns the
-// exclusive prefix and sets `total` (same in every thread).
-__device__ __forceinline__ int block_exclusive_scan_256(int v, int& total, int* warp_s) {
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int incl = warp_inclusive_scan(v);
-  __syncthreads();  // warp_s may still be read by a previous call
-  if (lane == 31) warp_s[warp] = incl;
-  __syncthreads();
-  int wpre = 0, tot = 0;
-#pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    const int x = warp_s[i];
-    wpre += i < warp ? x : 0;
-    tot += x;
-  }
-  total = tot;
-  return wpre + incl - v;
 }
 
 // One warp per expert (eight per CTA): the exclusive running sum of the
@@ -180,8 +155,8 @@ __global__ void __launch_bounds__(32 * kScanWarps) scan_kernel(
     const int v = i < E ? __ldcg(kept_g + i) : 0;
     const int d = i < E ? __ldcg(drop_g + i) : 0;
     int tot, dtot;
-    const int ex = block_exclusive_scan_256(v, tot, warp_s);
-    block_exclusive_scan_256(d, dtot, warp_s);
+    const int ex = block_exclusive_scan(v, tot, warp_s);
+    block_exclusive_scan(d, dtot, warp_s);
     if (i < E) expert_off[i] = carry_off + ex;
     if (i < E && i % G == 0) rank_off[i / G] = carry_off + ex;
     carry_off += tot;
@@ -300,10 +275,12 @@ __global__ void __launch_bounds__(512) scatter_code_kernel(const DispatchArgs a,
   };
   int64_t t = blockIdx.x;
   // Before the wait: x and the pair data of the count kernel (two launches
-  // back) only; tile bases and offsets come from the scan just before.
+  // back, unless pairs_early is 0) only; tile bases and offsets come from the
+  // scan just before.
   uint4 cur[2 * G];
   ld_tok(t, cur);
   PairA a0{-1, -1}, a1{-1, -1}, a_next2{-1, -1};
+  if (!a.pairs_early) pdl_wait();
   if (slot) {
     a0 = pair_load_a(a, t, c);
     a1 = pair_load_a(a, t + GS, c);
@@ -382,6 +359,7 @@ __global__ void __launch_bounds__(256) scatter_bf16_kernel(const DispatchArgs a,
   char* const pbase = static_cast<char*>(a.payload);
 
   PairA a0{-1, -1}, a1{-1, -1}, a_next2{-1, -1};
+  if (!a.pairs_early) pdl_wait();
   if (slot) {  // before the wait: pair data of the count kernel, two launches back
     a0 = pair_load_a(a, w0, lane);
     a1 = pair_load_a(a, w0 + W, lane);
@@ -490,8 +468,13 @@ cudaError_t launch_layout_from_bitmap(const DispatchArgs& a, const uint32_t* bit
 }
 
 cudaError_t launch_scan_scatter(const DispatchArgs& a, int sms, cudaStream_t s) {
-  cudaError_t err = launch_scan(a, s);
+  const cudaError_t err = launch_scan(a, s);
   if (err != cudaSuccess) return err;
+  return launch_scatter(a, sms, s);
+}
+
+cudaError_t launch_scatter(const DispatchArgs& a, int sms, cudaStream_t s) {
+  cudaError_t err = cudaSuccess;
   if (a.T == 0) return cudaSuccess;
 
   const int tile_log2 = __builtin_ctz(static_cast<unsigned>(a.tile));

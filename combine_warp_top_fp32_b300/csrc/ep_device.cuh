@@ -82,6 +82,51 @@ __device__ __forceinline__ int warp_inclusive_scan(int v) {
   return v;
 }
 
+// Exclusive scan of one value per thread over the block (at most 32 warps);
+// returns the exclusive prefix and sets `total` (same in every thread).
+// warp_s holds one int per warp.
+__device__ __forceinline__ int block_exclusive_scan(int v, int& total, int* warp_s) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
+  const int incl = warp_inclusive_scan(v);
+  __syncthreads();  // warp_s may still be read by a previous call
+  if (lane == 31) warp_s[warp] = incl;
+  __syncthreads();
+  int wpre = 0, tot = 0;
+  for (int i = 0; i < nw; ++i) {
+    const int x = warp_s[i];
+    wpre += i < warp ? x : 0;
+    tot += x;
+  }
+  total = tot;
+  return wpre + incl - v;
+}
+
+// Per-tile expert masks mask[e][w] (bit b of word w: token 32w+b of the tile
+// chose e; TW words per expert, TW a power of two <= 32): pre[e][w] = set bits
+// of e in the words before w, and tile_counts[e * ntiles + b] = set bits in
+// the whole tile. One thread per (e, w) and a segmented warp scan of log2(TW)
+// steps; the loop bound is the same for the whole block, so every lane takes
+// part in every shuffle (blockDim a multiple of 32).
+__device__ __forceinline__ void tile_word_prefix(const uint32_t* mask, uint32_t* pre, int E, int TW,
+                                                 int32_t* __restrict__ tile_counts, int ntiles, int b) {
+  const int lane = threadIdx.x & 31;
+  const int n = E * TW;
+  for (int i0 = 0; i0 < n; i0 += blockDim.x) {
+    const int i = i0 + threadIdx.x;
+    const bool ok = i < n;
+    const int c = ok ? __popc(mask[i]) : 0;
+    int v = c;
+    for (int o = 1; o < TW; o <<= 1) {
+      const int u = __shfl_up_sync(0xffffffffu, v, o);
+      if ((lane & (TW - 1)) >= o) v += u;
+    }
+    if (ok) {
+      pre[i] = static_cast<uint32_t>(v - c);
+      if ((i & (TW - 1)) == TW - 1) tile_counts[static_cast<int64_t>(i / TW) * ntiles + b] = v;
+    }
+  }
+}
+
 // ---- per-token int8 code of 16 consecutive elements --------------------------
 // scale = amax / 127 (IEEE division); q = clamp(rint(x / scale), -127, 127)
 // with IEEE division and ties-to-even; scale == 0 codes every element as 0.

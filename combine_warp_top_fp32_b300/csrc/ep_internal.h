@@ -99,6 +99,10 @@ struct DispatchArgs {
   uint32_t* ticket;
   int32_t *kept, *dropped, *tile_counts, *tile_base, *lrank;
   int tile, ntiles;
+  // 1 when the pair data (topk_idx, lrank) was written two or more launches
+  // before the scatter, which may then read it before its dependency wait;
+  // 0 when the kernel just before the scatter wrote it.
+  int pairs_early = 1;
 };
 
 // ep_dispatch: count kernel, then scan and scatter.
@@ -113,6 +117,8 @@ cudaError_t launch_bitmap_layout(const DispatchArgs& a, const uint32_t* bitmap, 
 // The scan and the scatter alone, once tile_counts / lrank are written (by
 // the count kernel or the fused route+count kernel) and the ticket is clear.
 cudaError_t launch_scan_scatter(const DispatchArgs& a, int sms, cudaStream_t s);
+// The scatter alone, once lrank, tile_base and the offsets are written.
+cudaError_t launch_scatter(const DispatchArgs& a, int sms, cudaStream_t s);
 
 // Routing fused with the dispatch's per-tile count (ep_route_dispatch).
 struct RouteCountArgs {
@@ -124,6 +130,16 @@ struct RouteCountArgs {
   uint32_t* ticket;
 };
 cudaError_t launch_route_count(const RouteCountArgs& r, cudaStream_t s);
+
+// Small batches (at most kClusterTiles tiles of 32 tokens, E <= 256): one
+// thread-block cluster of one CTA per tile routes the batch and forms the
+// whole layout (topk_idx / topk_w, lrank, tile_base and every layout output)
+// in one launch; the scatter follows. Returns cudaErrorNotSupported when the
+// batch is not small.
+constexpr int kClusterTiles = 8;      // the portable cluster size
+constexpr int kClusterExperts = 256;  // experts per routing lane group of 32: at most 8 values per lane
+bool small_batch(int T, int E, int tile);
+cudaError_t launch_route_layout_small(const RouteCountArgs& r, const DispatchArgs& a, cudaStream_t s);
 
 struct CombineArgs {
   int T, H, k;

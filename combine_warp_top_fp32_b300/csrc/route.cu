@@ -432,37 +432,21 @@ __global__ void __launch_bounds__(256) route_topk_kernel(const float* __restrict
   }
 }
 
-// Routing fused with the per-tile count of the dispatch (the ThunderEP
-// article's §5.2 suggestion to bucket by destination while routing): CTA b
-// routes the tokens of tile b = [b*tile, (b+1)*tile), writes their slots,
-// and builds the tile's per-expert bit masks in shared memory, from which it
-// writes the tile's count per expert and each pair's rank within the tile in
-// token order (the same tile_counts / lrank as the dispatch's count kernel).
+// Routes the nt tokens of the tile starting at token t0 (one L-lane group
+// per token; two tokens per warp in flight when L = 32 and VPL <= 4), writes
+// their slots and sets their bits in the tile's per-expert masks in shared
+// memory: mask[e][w] bit b = token 32w+b of the tile chose e. The masks must
+// be zero on entry; the caller synchronises the CTA afterwards.
 template <int VPL, bool VEC4>
-__global__ void __launch_bounds__(VPL >= 16 ? 256 : 512) route_count_kernel(
-    const float* __restrict__ logits, int T, int E, int k, int lanes_log2, int renorm, int tile, int ntiles,
-    int32_t* __restrict__ topk_idx, float* __restrict__ topk_w, int32_t* __restrict__ tile_counts,
-    int32_t* __restrict__ lrank, uint32_t* ticket) {
-  extern __shared__ uint32_t smem[];
+__device__ __forceinline__ void route_tile(const float* __restrict__ logits, int64_t t0, int nt, int E, int k,
+                                           int lanes_log2, int renorm, int TW, uint32_t* mask,
+                                           int32_t* __restrict__ topk_idx, float* __restrict__ topk_w) {
   const int L = 1 << lanes_log2;
   const int lane = threadIdx.x & 31;
   const int sub = lane & (L - 1);
   const int groups_per_warp = 32 >> lanes_log2;
   const int grp = lane >> lanes_log2;
   const int warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
-  const int TW = tile >> 5;
-  uint32_t* mask = smem;          // [E][TW] bit b of word w: token 32*w+b of the tile chose e
-  uint32_t* pre = smem + E * TW;  // [E][TW] set bits of e in the words before w
-  const int b = blockIdx.x;
-  const int64_t t0 = static_cast<int64_t>(b) * tile;
-  const int nt = static_cast<int>(min(static_cast<int64_t>(tile), T - t0));
-  for (int i = threadIdx.x; i < E * TW; i += blockDim.x) mask[i] = 0u;
-  pdl_wait();  // the logits may come from the kernel before this one
-  pdl_launch_dependents();
-  if (b == 0 && threadIdx.x == 0) *ticket = 0u;  // the scan that follows counts its CTAs from 0
-  __syncthreads();
-  if (nt <= 0) return;  // an empty batch: only the ticket
-
   bool routed = false;
   if constexpr (VPL <= 4) {
     if (L == 32) {  // two tokens per warp in flight: tile tokens w and w + nw
@@ -499,14 +483,36 @@ __global__ void __launch_bounds__(VPL >= 16 ? 256 : 512) route_count_kernel(
       }
     }
   }
+}
+
+// Routing fused with the per-tile count of the dispatch (the ThunderEP
+// article's §5.2 suggestion to bucket by destination while routing): CTA b
+// routes the tokens of tile b = [b*tile, (b+1)*tile), writes their slots,
+// and builds the tile's per-expert bit masks in shared memory, from which it
+// writes the tile's count per expert and each pair's rank within the tile in
+// token order (the same tile_counts / lrank as the dispatch's count kernel).
+template <int VPL, bool VEC4>
+__global__ void __launch_bounds__(VPL >= 16 ? 256 : 512) route_count_kernel(
+    const float* __restrict__ logits, int T, int E, int k, int lanes_log2, int renorm, int tile, int ntiles,
+    int32_t* __restrict__ topk_idx, float* __restrict__ topk_w, int32_t* __restrict__ tile_counts,
+    int32_t* __restrict__ lrank, uint32_t* ticket) {
+  extern __shared__ uint32_t smem[];
+  const int TW = tile >> 5;
+  uint32_t* mask = smem;          // [E][TW] bit b of word w: token 32*w+b of the tile chose e
+  uint32_t* pre = smem + E * TW;  // [E][TW] set bits of e in the words before w
+  const int b = blockIdx.x;
+  const int64_t t0 = static_cast<int64_t>(b) * tile;
+  const int nt = static_cast<int>(min(static_cast<int64_t>(tile), T - t0));
+  for (int i = threadIdx.x; i < E * TW; i += blockDim.x) mask[i] = 0u;
+  pdl_wait();  // the logits may come from the kernel before this one
+  pdl_launch_dependents();
+  if (b == 0 && threadIdx.x == 0) *ticket = 0u;  // the scan that follows counts its CTAs from 0
+  __syncthreads();
+  if (nt <= 0) return;  // an empty batch: only the ticket
+  route_tile<VPL, VEC4>(logits, t0, nt, E, k, lanes_log2, renorm, TW, mask, topk_idx, topk_w);
   __syncthreads();
 
-  for (int e = warp; e < E; e += nw) {
-    const int c = lane < TW ? __popc(mask[e * TW + lane]) : 0;
-    const int incl = warp_inclusive_scan(c);
-    if (lane < TW) pre[e * TW + lane] = static_cast<uint32_t>(incl - c);
-    if (lane == 31) tile_counts[static_cast<int64_t>(e) * ntiles + b] = incl;
-  }
+  tile_word_prefix(mask, pre, E, TW, tile_counts, ntiles, b);
   __syncthreads();
 
   const int64_t base = t0 * k;
@@ -516,6 +522,131 @@ __global__ void __launch_bounds__(VPL >= 16 ? 256 : 512) route_count_kernel(
     const int w = tl >> 5;
     lrank[base + p] = static_cast<int>(pre[e * TW + w]) + __popc(mask[e * TW + w] & ((1u << (tl & 31)) - 1u));
   }
+}
+
+// ---- thread-block cluster helpers (distributed shared memory) ----
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.aligned;" ::: "memory"); }
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// Address of `p` (this CTA's shared memory) in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t cluster_map(const void* p, uint32_t rank) {
+  const uint32_t local = static_cast<uint32_t>(__cvta_generic_to_shared(p));
+  uint32_t remote;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(local), "r"(rank));
+  return remote;
+}
+__device__ __forceinline__ void st_cluster_u32(uint32_t addr, uint32_t v) {
+  asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+
+// Small batches (at most kClusterTiles tiles of 32 tokens): one cluster of
+// one CTA per tile, a warp per token. Each CTA routes its tile and ranks its
+// pairs as route_count_kernel does, but pushes its per-expert tile counts
+// into CTA 0's shared memory instead of global memory; after a cluster
+// barrier CTA 0 alone forms what the scan kernel would from them (tile bases,
+// raw and kept counts, expert and rank offsets, the number dropped), so the
+// whole layout costs one launch. The outputs are those of route_count_kernel
+// + scan_kernel, bit for bit.
+template <int VPL, bool VEC4>
+__global__ void __launch_bounds__(1024, 1) route_layout_cluster_kernel(
+    const float* __restrict__ logits, int T, int E, int k, int lanes_log2, int renorm, int R, int cap,
+    int32_t* __restrict__ topk_idx, float* __restrict__ topk_w, int32_t* __restrict__ lrank,
+    int32_t* __restrict__ tile_base, int32_t* __restrict__ expert_counts, int32_t* __restrict__ expert_raw,
+    int32_t* __restrict__ expert_off, int32_t* __restrict__ rank_off, int32_t* __restrict__ n_dropped) {
+  extern __shared__ uint32_t smem[];
+  const int C = gridDim.x;  // tiles = CTAs = the cluster
+  uint32_t* mask = smem;                                // [E] this tile's word per expert
+  int* counts_s = reinterpret_cast<int*>(smem + E);    // [E][C] (CTA 0) every tile's count per expert
+  int* kept_s = counts_s + E * C;                      // [E] (CTA 0)
+  int* drop_s = kept_s + E;                            // [E] (CTA 0)
+  int* warp_s = drop_s + E;                            // [32] (CTA 0)
+  const int lane = threadIdx.x & 31;
+  const int warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  const int b = blockIdx.x;
+  const int64_t t0 = static_cast<int64_t>(b) * 32;
+  const int nt = min(32, T - static_cast<int>(t0));  // >= 1: the grid has ceil(T/32) CTAs
+  for (int i = threadIdx.x; i < E; i += blockDim.x) mask[i] = 0u;
+  cluster_arrive_relaxed();  // CTA 0 must be running before anyone writes into it
+  pdl_wait();                // the logits may come from the kernel before this one
+  pdl_launch_dependents();
+  __syncthreads();
+  route_tile<VPL, VEC4>(logits, t0, nt, E, k, lanes_log2, renorm, 1, mask, topk_idx, topk_w);
+  __syncthreads();
+
+  cluster_wait();
+  const uint32_t counts0 = cluster_map(counts_s, 0);
+  for (int e = threadIdx.x; e < E; e += blockDim.x)
+    st_cluster_u32(counts0 + 4u * static_cast<uint32_t>(e * C + b), static_cast<uint32_t>(__popc(mask[e])));
+  const int64_t base = t0 * k;
+  for (int p = threadIdx.x; p < nt * k; p += blockDim.x) {
+    const int e = topk_idx[base + p];  // written above by this CTA
+    const int tl = p / k;
+    lrank[base + p] = __popc(mask[e] & ((1u << tl) - 1u));
+  }
+  cluster_sync();  // every tile's counts are in CTA 0
+  if (b != 0) return;
+
+  for (int e = warp; e < E; e += nw) {
+    const int c = lane < C ? counts_s[e * C + lane] : 0;
+    const int incl = warp_inclusive_scan(c);
+    if (lane < C) tile_base[e * C + lane] = incl - c;
+    if (lane == 31) {
+      const int kept = min(incl, cap);
+      expert_counts[e] = kept;
+      if (expert_raw) expert_raw[e] = incl;
+      kept_s[e] = kept;
+      drop_s[e] = incl - kept;
+    }
+  }
+  __syncthreads();
+  const int G = E / R;  // rank r starts at its first expert r*G
+  int carry = 0, drops = 0;
+  for (int c0 = 0; c0 < E; c0 += blockDim.x) {
+    const int i = c0 + threadIdx.x;
+    const int v = i < E ? kept_s[i] : 0;
+    const int d = i < E ? drop_s[i] : 0;
+    int tot, dtot;
+    const int ex = block_exclusive_scan(v, tot, warp_s);
+    block_exclusive_scan(d, dtot, warp_s);
+    if (i < E) expert_off[i] = carry + ex;
+    if (i < E && i % G == 0) rank_off[i / G] = carry + ex;
+    carry += tot;
+    drops += dtot;
+  }
+  if (threadIdx.x == 0) {
+    expert_off[E] = carry;
+    rank_off[R] = carry;
+    *n_dropped = drops;
+  }
+}
+
+template <int VPL, bool VEC4>
+cudaError_t launch_route_layout_cluster_t(const RouteCountArgs& r, const DispatchArgs& a, int lanes_log2,
+                                          cudaStream_t s) {
+  constexpr int kBlock = 1024;  // a warp per token of the tile
+  const int C = (r.T + 31) / 32;
+  const int smem = (r.E + r.E * C + 2 * r.E + 32) * static_cast<int>(sizeof(uint32_t));  // <= 12.1 KB
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(C));
+  cfg.blockDim = dim3(kBlock);
+  cfg.dynamicSmemBytes = static_cast<size_t>(smem);
+  cfg.stream = s;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = static_cast<unsigned>(C);
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  return cudaLaunchKernelEx(&cfg, route_layout_cluster_kernel<VPL, VEC4>, r.logits, r.T, r.E, r.k, lanes_log2,
+                            r.renorm, a.R, a.cap, r.topk_idx, r.topk_w, a.lrank, a.tile_base, a.expert_counts,
+                            a.expert_raw, a.expert_off, a.rank_off, a.n_dropped);
 }
 
 template <int VPL, bool VEC4>
@@ -602,6 +733,29 @@ cudaError_t launch_route_count(const RouteCountArgs& r, cudaStream_t s) {
   if (vpl <= 8) return launch_route_count_t<8, false>(r, lanes_log2, s);
   if (vpl <= 16) return launch_route_count_t<16, false>(r, lanes_log2, s);
   return launch_route_count_t<32, false>(r, lanes_log2, s);
+}
+
+}  // namespace ep
+
+namespace ep {
+
+bool small_batch(int T, int E, int tile) {
+  return T > 0 && T <= 32 * kClusterTiles && E <= kClusterExperts && tile == 32;
+}
+
+cudaError_t launch_route_layout_small(const RouteCountArgs& r, const DispatchArgs& a, cudaStream_t s) {
+  if (!small_batch(r.T, r.E, r.tile)) return cudaErrorNotSupported;
+  int lanes_log2 = 0;
+  while ((1 << lanes_log2) < r.E && lanes_log2 < 5) ++lanes_log2;
+  const int L = 1 << lanes_log2;
+  const int vpl = (r.E + L - 1) / L;  // <= 8 for E <= 256
+  const bool vec4 = (L == 32) && (r.E % 128 == 0);
+  if (vec4) return vpl == 4 ? launch_route_layout_cluster_t<4, true>(r, a, lanes_log2, s)
+                            : launch_route_layout_cluster_t<8, true>(r, a, lanes_log2, s);
+  if (vpl <= 1) return launch_route_layout_cluster_t<1, false>(r, a, lanes_log2, s);
+  if (vpl <= 2) return launch_route_layout_cluster_t<2, false>(r, a, lanes_log2, s);
+  if (vpl <= 4) return launch_route_layout_cluster_t<4, false>(r, a, lanes_log2, s);
+  return launch_route_layout_cluster_t<8, false>(r, a, lanes_log2, s);
 }
 
 }  // namespace ep

@@ -204,6 +204,12 @@ EDGE = [
     (3000, 128, 32, 4, 4, 0.25, 1, 0, "heavy capacity drops"),
     (2048, 256, 64, 6, 8, 1.0, 0, 1, "capacity factor 1.0, bf16"),
     (40000, 16, 512, 4, 8, 1.0, 1, 0, "many experts x tiles (80,384 tile counts)"),
+    (256, 64, 256, 8, 8, 0.5, 1, 1, "largest batch laid out by one cluster (8 tiles), E=256, drops"),
+    (257, 64, 256, 8, 8, 0.0, 0, 0, "one token past the cluster layout"),
+    (200, 32, 257, 3, 1, 0.0, 1, 0, "E=257: past the cluster layout's expert limit"),
+    (100, 32, 160, 5, 8, 0.3, 0, 0, "cluster layout, 5 values per lane, ragged tile, drops"),
+    (250, 64, 64, 6, 8, 0.0, 2, 0, "cluster layout, two tokens per warp in flight"),
+    (33, 48, 3, 3, 3, 0.0, 1, 1, "cluster layout of two tiles, one token in the second"),
 ]
 
 
