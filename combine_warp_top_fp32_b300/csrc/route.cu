@@ -563,9 +563,8 @@ __global__ void __launch_bounds__(1024, 1) route_layout_cluster_kernel(
   int* counts_s = reinterpret_cast<int*>(smem + E);    // [E][C] (CTA 0) every tile's count per expert
   int* kept_s = counts_s + E * C;                      // [E] (CTA 0)
   int* drop_s = kept_s + E;                            // [E] (CTA 0)
-  int* warp_s = drop_s + E;                            // [32] (CTA 0)
   const int lane = threadIdx.x & 31;
-  const int warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  const int warp = threadIdx.x >> 5;
   const int b = blockIdx.x;
   const int64_t t0 = static_cast<int64_t>(b) * 32;
   const int nt = min(32, T - static_cast<int>(t0));  // >= 1: the grid has ceil(T/32) CTAs
@@ -590,37 +589,58 @@ __global__ void __launch_bounds__(1024, 1) route_layout_cluster_kernel(
   cluster_sync();  // every tile's counts are in CTA 0
   if (b != 0) return;
 
-  for (int e = warp; e < E; e += nw) {
-    const int c = lane < C ? counts_s[e * C + lane] : 0;
-    const int incl = warp_inclusive_scan(c);
-    if (lane < C) tile_base[e * C + lane] = incl - c;
-    if (lane == 31) {
-      const int kept = min(incl, cap);
+  // one thread per (expert, tile), segments of Cp lanes (C rounded up to a
+  // power of two, the padding lanes adding 0): a segmented scan gives the
+  // tile bases, and the segment's last lane the expert's raw total
+  int Cp = 1;
+  while (Cp < C) Cp <<= 1;
+  for (int i0 = 0; i0 < E * Cp; i0 += blockDim.x) {
+    const int i = i0 + threadIdx.x;
+    const int e = i / Cp, w = i & (Cp - 1);  // w == lane & (Cp - 1): i0 is a multiple of 32
+    const bool ok = i < E * Cp && w < C;
+    const int c = ok ? counts_s[e * C + w] : 0;
+    int v = c;
+    for (int o = 1; o < Cp; o <<= 1) {
+      const int u = __shfl_up_sync(0xffffffffu, v, o);
+      if (w >= o) v += u;
+    }
+    if (ok) tile_base[e * C + w] = v - c;
+    if (i < E * Cp && w == Cp - 1) {
+      const int kept = min(v, cap);
       expert_counts[e] = kept;
-      if (expert_raw) expert_raw[e] = incl;
+      if (expert_raw) expert_raw[e] = v;
       kept_s[e] = kept;
-      drop_s[e] = incl - kept;
+      drop_s[e] = v - kept;
     }
   }
   __syncthreads();
+  if (warp != 0) return;
+
+  // expert and rank offsets, one warp: lane l sums experts [l*per, (l+1)*per)
   const int G = E / R;  // rank r starts at its first expert r*G
-  int carry = 0, drops = 0;
-  for (int c0 = 0; c0 < E; c0 += blockDim.x) {
-    const int i = c0 + threadIdx.x;
-    const int v = i < E ? kept_s[i] : 0;
-    const int d = i < E ? drop_s[i] : 0;
-    int tot, dtot;
-    const int ex = block_exclusive_scan(v, tot, warp_s);
-    block_exclusive_scan(d, dtot, warp_s);
-    if (i < E) expert_off[i] = carry + ex;
-    if (i < E && i % G == 0) rank_off[i / G] = carry + ex;
-    carry += tot;
-    drops += dtot;
+  const int per = (E + 31) / 32;
+  const int e0 = lane * per;
+  int kv = 0, dv = 0;
+  for (int j = 0; j < per; ++j)
+    if (e0 + j < E) {
+      kv += kept_s[e0 + j];
+      dv += drop_s[e0 + j];
+    }
+  const int ki = warp_inclusive_scan(kv);
+  const int di = warp_inclusive_scan(dv);
+  int run = ki - kv;
+  for (int j = 0; j < per; ++j) {
+    const int e = e0 + j;
+    if (e < E) {
+      expert_off[e] = run;
+      if (e % G == 0) rank_off[e / G] = run;
+      run += kept_s[e];
+    }
   }
-  if (threadIdx.x == 0) {
-    expert_off[E] = carry;
-    rank_off[R] = carry;
-    *n_dropped = drops;
+  if (lane == 31) {
+    expert_off[E] = ki;
+    rank_off[R] = ki;
+    *n_dropped = di;
   }
 }
 
@@ -629,7 +649,7 @@ cudaError_t launch_route_layout_cluster_t(const RouteCountArgs& r, const Dispatc
                                           cudaStream_t s) {
   constexpr int kBlock = 1024;  // a warp per token of the tile
   const int C = (r.T + 31) / 32;
-  const int smem = (r.E + r.E * C + 2 * r.E + 32) * static_cast<int>(sizeof(uint32_t));  // <= 12.1 KB
+  const int smem = (r.E + r.E * C + 2 * r.E) * static_cast<int>(sizeof(uint32_t));  // <= 11 KB
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(C));
   cfg.blockDim = dim3(kBlock);
