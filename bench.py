@@ -408,6 +408,52 @@ def run_gpu(args):
                     "combine": "combine_kernel<bf16>"}
     traffic = recorded_traffic(dominant, w.name, args.payload)
 
+    # int8 in both directions, beside the headline (not in place of it): the
+    # experts return int8 rows + per-row scales (ep_quantize_rows of the same
+    # expert outputs), which the combine dequantises. Same graph timing.
+    both = None
+    if p8 == PAYLOAD_MODE["int8"] and w.T > 0 and not args.no_int8_return:
+        eo_q = torch.empty(eo.shape, dtype=torch.int8, device=dev)
+        eo_s = torch.empty(eo.shape[0], dtype=torch.float32, device=dev)
+        ep.ep_quantize_rows(eo, eo_q, eo_s)
+
+        def step_q():
+            if args.path == "fused":
+                buf.route_dispatch(logits, x)
+            else:
+                buf.route(logits)
+                buf.dispatch(x)
+            buf.combine(eo_q, eo_s)
+
+        warm = torch.cuda.Stream()
+        warm.wait_stream(stream)
+        with torch.cuda.stream(warm):
+            step_q()
+        stream.wait_stream(warm)
+        gq = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gq):
+            for _ in range(args.steps):
+                step_q()
+        gq.replay()
+        torch.cuda.synchronize()
+        q0, q1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        barrier()
+        torch.cuda.synchronize()
+        q0.record(stream)
+        gq.replay()
+        q1.record(stream)
+        torch.cuda.synchronize()
+        barrier()
+        assert ep.ep_get_error(buf.ws) == ep.EP_OK
+        q_s = max_over_ranks(q0.elapsed_time(q1) / 1e3)
+        nbq = algorithmic_bytes(w.T, w.H, w.E, w.k, N, True, out_int8=True)
+        q_gbs = nbq["total"] / (q_s / args.steps) / 1e9
+        both = {"ms_per_step": 1e3 * q_s / args.steps, "value": w.T * args.steps * world / q_s, "unit": "tokens/s",
+                "bytes_per_step": nbq["total"], "gbs": q_gbs, "frac_of_8000": q_gbs / NOMINAL_HBM_GBS,
+                f"frac_of_{peak_src}": q_gbs / peak,
+                "note": "expert outputs returned as int8 + fp32 row scales (ep_quantize_rows), dequantised by the combine"}
+        del eo_q, eo_s, gq
+
     # end to end through the public API with host buffers: pinned H2D of the
     # step's inputs (logits, x), the calls, D2H of the result y, every step.
     # The expert outputs stay the device-resident stand-in of the timed steps:
@@ -499,6 +545,8 @@ def run_gpu(args):
             "e2e": e2e,
             "cpu_baseline": cpu_baseline,
         }
+        if both is not None:
+            line["int8_both_directions"] = both
         print(json.dumps(line))
     if world > 1:
         dist.destroy_process_group()
@@ -646,6 +694,8 @@ def parse_args(argv=None):
     ap.add_argument("--eager", action="store_true", help="launch through the binding each step (no CUDA graph)")
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-int8-return", action="store_true",
+                    help="skip the extra line with int8 expert outputs (int8 payload only)")
     ap.add_argument("--cpu-baseline-s", type=float, default=15.0)
     ap.add_argument("--reference-step-s", type=float, default=2.0)
     args = ap.parse_args(argv)

@@ -16,10 +16,13 @@
 //   - a ballot drops the dropped slots and the kept ones are gathered, in
 //     slot order, into registers of every lane (row address, weight, scale),
 //     so a token with few kept slots costs only their loads;
-//   - the row is walked in 16-byte chunks per lane (8 bf16 or 16 int8
-//     elements); the loads of all kept slots for several chunks are issued
-//     back to back before any arithmetic, 16 per lane in flight whatever the
-//     number of kept slots (2 slots x 8 chunks, 4 x 4 or 8 x 2);
+//   - the row is walked in 16-byte chunks per lane (8 bf16, 16 int8 / E4M3
+//     or 32 int4 elements); the loads of all kept slots for several chunks
+//     are issued back to back before any arithmetic, a fixed number per lane
+//     in flight whatever the number of kept slots (bf16: 16 = 2 slots x 8
+//     chunks, 4 x 4 or 8 x 2; coded rows: 8);
+//   - the arithmetic runs on packed pairs of elements (f32x2), and coded
+//     rows are widened by integer operations, not the conversion unit;
 //   - more than 8 kept slots (k > 8) are taken in groups of 8 in slot order,
 //     with the accumulators carried across groups, so the order of the fmas is
 //     the same in every case.
@@ -36,56 +39,84 @@ struct Chunk {
   static constexpr int kElems = FMT == kFmtBf16 ? 8 : (FMT == kFmtInt4 ? 32 : 16);
 };
 
-// acc[0..EL) += w * v for one 16-byte chunk of a kept row, in element order;
-// v = float(bf16), or (float)code * scale with the int8 or E4M3 code widened
-// exactly.
+// Float whose low mantissa byte is byte i of b: 2^23 + byte (a byte permute).
+__device__ __forceinline__ uint32_t magic_byte(uint32_t b, int i) {
+  return __byte_perm(b, 0x4B000000u, 0x7440u | static_cast<unsigned>(i));
+}
+
+__device__ __forceinline__ uint64_t splat2(float v) { return f32x2_pack(__float_as_uint(v), __float_as_uint(v)); }
+
+// acc[0..EL/2) += w * v for one 16-byte chunk of a kept row: the accumulators
+// are packed pairs of consecutive elements (element 2j in the low half) and
+// every step is a packed add / mul / fma .rn.f32x2, the same IEEE operation
+// per element as its scalar form: fmaf(w, v, acc) with v = float(bf16), or
+// v = (float)code * scale with the code widened exactly by integer operations
+// only (no conversion unit):
+//   bf16:  the halfword shifted into the top of a float;
+//   int8:  byte ^ 0x80 = q + 128 as the low byte of 2^23, minus 2^23 + 128;
+//   int4:  nibble ^ 8 = q + 8 (bytes of lo/hi nibbles), minus 2^23 + 8;
+//   E4M3:  the code's exponent and mantissa moved to float bits 20..26 and its
+//          sign to bit 31 is the value times 2^-120 (subnormal codes land on
+//          float subnormals), scaled back by 2^120 exactly. The NaN codes 0x7F
+//          / 0xFF, which no encoder here writes, read as +-480.
 template <int FMT>
-__device__ __forceinline__ void fma_chunk(float* acc, uint4 v, float w, float sc) {
-  if constexpr (FMT == kFmtInt8) {
-    const uint32_t u[4] = {v.x, v.y, v.z, v.w};
+__device__ __forceinline__ void fma_chunk(uint64_t* acc, uint4 v, uint64_t w2, uint64_t s2) {
+  const uint32_t u[4] = {v.x, v.y, v.z, v.w};
+  if constexpr (FMT == kFmtBf16) {
 #pragma unroll
-    for (int q = 0; q < 4; ++q)
-#pragma unroll
-      for (int i = 0; i < 4; ++i) acc[4 * q + i] = __fmaf_rn(w, __fmul_rn(i8_at(u[q], i), sc), acc[4 * q + i]);
-  } else if constexpr (FMT == kFmtInt4) {
-    const uint32_t u[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-    for (int q = 0; q < 4; ++q)
-#pragma unroll
-      for (int i = 0; i < 8; ++i) acc[8 * q + i] = __fmaf_rn(w, __fmul_rn(i4_at(u[q], i), sc), acc[8 * q + i]);
-  } else if constexpr (FMT == kFmtFp8) {
-    const uint32_t u[4] = {v.x, v.y, v.z, v.w};
+    for (int q = 0; q < 4; ++q) acc[q] = f32x2_fma(w2, f32x2_pack(u[q] << 16, u[q] & 0xffff0000u), acc[q]);
+  } else if constexpr (FMT == kFmtInt8) {
+    const uint64_t c2 = splat2(-8388736.0f);  // -(2^23 + 128)
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
-      float f[4];
-      e4m3x2_to_f32(u[q] & 0xffffu, f[0], f[1]);
-      e4m3x2_to_f32(u[q] >> 16, f[2], f[3]);
+      const uint32_t b = u[q] ^ 0x80808080u;
 #pragma unroll
-      for (int i = 0; i < 4; ++i) acc[4 * q + i] = __fmaf_rn(w, __fmul_rn(f[i], sc), acc[4 * q + i]);
+      for (int j = 0; j < 2; ++j) {
+        const uint64_t f2 = f32x2_pack(magic_byte(b, 2 * j), magic_byte(b, 2 * j + 1));
+        acc[2 * q + j] = f32x2_fma(w2, f32x2_mul(f32x2_add(f2, c2), s2), acc[2 * q + j]);
+      }
     }
-  } else {
-    acc[0] = __fmaf_rn(w, bf16_lo(v.x), acc[0]);
-    acc[1] = __fmaf_rn(w, bf16_hi(v.x), acc[1]);
-    acc[2] = __fmaf_rn(w, bf16_lo(v.y), acc[2]);
-    acc[3] = __fmaf_rn(w, bf16_hi(v.y), acc[3]);
-    acc[4] = __fmaf_rn(w, bf16_lo(v.z), acc[4]);
-    acc[5] = __fmaf_rn(w, bf16_hi(v.z), acc[5]);
-    acc[6] = __fmaf_rn(w, bf16_lo(v.w), acc[6]);
-    acc[7] = __fmaf_rn(w, bf16_hi(v.w), acc[7]);
+  } else if constexpr (FMT == kFmtInt4) {
+    const uint64_t c2 = splat2(-8388616.0f);  // -(2^23 + 8)
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const uint32_t lo = (u[q] & 0x0F0F0F0Fu) ^ 0x08080808u;         // nibbles 0, 2, 4, 6
+      const uint32_t hi = ((u[q] >> 4) & 0x0F0F0F0Fu) ^ 0x08080808u;  // nibbles 1, 3, 5, 7
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const uint64_t f2 = f32x2_pack(magic_byte(lo, j), magic_byte(hi, j));
+        acc[4 * q + j] = f32x2_fma(w2, f32x2_mul(f32x2_add(f2, c2), s2), acc[4 * q + j]);
+      }
+    }
+  } else {  // E4M3
+    const uint64_t e2 = f32x2_pack(0x7B800000u, 0x7B800000u);  // 2^120
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      uint32_t r[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i)  // byte i to the top, then an arithmetic shift by 4
+        r[i] = static_cast<uint32_t>(static_cast<int32_t>(u[q] << (24 - 8 * i)) >> 4) & 0x87F00000u;
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        const uint64_t f2 = f32x2_mul(f32x2_pack(r[2 * j], r[2 * j + 1]), e2);
+        acc[2 * q + j] = f32x2_fma(w2, f32x2_mul(f2, s2), acc[2 * q + j]);
+      }
+    }
   }
 }
 
-// Round EL fp32 accumulators to bf16 (RNE) and store them at y (16-byte aligned).
+// Round EL fp32 accumulators (EL/2 packed pairs) to bf16 (RNE) and store them
+// at y (16-byte aligned).
 template <int EL>
-__device__ __forceinline__ void store_bf16(char* y, const float* acc) {
+__device__ __forceinline__ void store_bf16(char* y, const uint64_t* acc) {
 #pragma unroll
   for (int s = 0; s < EL / 8; ++s) {
-    uint4 o;
-    o.x = pack_bf16x2_rn(acc[8 * s + 0], acc[8 * s + 1]);
-    o.y = pack_bf16x2_rn(acc[8 * s + 2], acc[8 * s + 3]);
-    o.z = pack_bf16x2_rn(acc[8 * s + 4], acc[8 * s + 5]);
-    o.w = pack_bf16x2_rn(acc[8 * s + 6], acc[8 * s + 7]);
-    st_v4(y + 16 * s, o);
+    uint32_t o[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      o[j] = pack_bf16x2_rn(__uint_as_float(static_cast<uint32_t>(acc[4 * s + j])),
+                            __uint_as_float(static_cast<uint32_t>(acc[4 * s + j] >> 32)));
+    st_v4(y + 16 * s, make_uint4(o[0], o[1], o[2], o[3]));
   }
 }
 
@@ -115,6 +146,12 @@ template <int FMT, int NS, int UNR>
 __device__ __forceinline__ void combine_token(int nk, int cbeg, int nchunk, int lane, const char* const (&p)[8],
                                               const float (&wv)[8], const float (&sv)[8], char* yrow) {
   constexpr int EL = Chunk<FMT>::kElems;
+  uint64_t w2[NS], s2[NS];
+#pragma unroll
+  for (int i = 0; i < NS; ++i) {
+    w2[i] = splat2(wv[i]);
+    s2[i] = splat2(sv[i]);
+  }
   for (int c0 = cbeg + lane; c0 < nchunk; c0 += 32 * UNR) {
     uint4 v[UNR][NS];
 #pragma unroll
@@ -127,12 +164,12 @@ __device__ __forceinline__ void combine_token(int nk, int cbeg, int nchunk, int 
 #pragma unroll
     for (int u = 0; u < UNR; ++u) {
       const int c = c0 + 32 * u;
-      float acc[EL];
+      uint64_t acc[EL / 2];
 #pragma unroll
-      for (int e = 0; e < EL; ++e) acc[e] = 0.f;
+      for (int e = 0; e < EL / 2; ++e) acc[e] = 0ull;
 #pragma unroll
       for (int i = 0; i < NS; ++i)
-        if (i < nk) fma_chunk<FMT>(acc, v[u][i], wv[i], sv[i]);
+        if (i < nk) fma_chunk<FMT>(acc, v[u][i], w2[i], s2[i]);
       if (c < nchunk) store_bf16<EL>(yrow + 2 * static_cast<int64_t>(c) * EL, acc);
     }
   }
@@ -140,8 +177,18 @@ __device__ __forceinline__ void combine_token(int nk, int cbeg, int nchunk, int 
 
 // LOADS = 16-byte loads in flight per lane: a token with few kept slots walks
 // more chunks per pass, so the bytes in flight do not shrink with drops.
+// int8 and E4M3 rows spend more instructions per byte than bf16 (widening,
+// the scale): they run 8 loads per lane with three CTAs per SM, which hides
+// the arithmetic better than 16 loads with two (int8 84.9 -> 74.8 us, E4M3
+// 121.8 -> 84.1 us on the capacity combine); int4 (32 elements per chunk)
+// keeps two.
+template <int FMT>
+constexpr int combine_min_ctas() {
+  return (FMT == kFmtInt8 || FMT == kFmtFp8) ? 3 : 2;
+}
+
 template <int FMT, int LOADS>
-__global__ void __launch_bounds__(256, 2) combine_kernel(const CombineArgs a) {
+__global__ void __launch_bounds__(256, combine_min_ctas<FMT>()) combine_kernel(const CombineArgs a) {
   constexpr int EL = Chunk<FMT>::kElems;
   constexpr bool kCoded = FMT != kFmtBf16;
   const int lane = threadIdx.x & 31;
@@ -207,9 +254,9 @@ __global__ void __launch_bounds__(256, 2) combine_kernel(const CombineArgs a) {
       // The loop bound is warp-uniform: the gathers shuffle across all lanes.
       for (int c0 = cbeg; c0 < cend; c0 += 32) {
         const int c = c0 + lane;
-        float acc[EL];
+        uint64_t acc[EL / 2];
 #pragma unroll
-        for (int e = 0; e < EL; ++e) acc[e] = 0.f;
+        for (int e = 0; e < EL / 2; ++e) acc[e] = 0ull;
         unsigned m = kept;
         while (m) {
           const int n = gather_group<FMT>(m, row, w, sc, base, row_bytes, p, wv, sv);
@@ -219,7 +266,7 @@ __global__ void __launch_bounds__(256, 2) combine_kernel(const CombineArgs a) {
             v[i] = (i < n && c < cend) ? ld_stream_v4(p[i] + 16 * static_cast<int64_t>(c)) : make_uint4(0, 0, 0, 0);
 #pragma unroll
           for (int i = 0; i < 8; ++i)
-            if (i < n) fma_chunk<FMT>(acc, v[i], wv[i], sv[i]);
+            if (i < n) fma_chunk<FMT>(acc, v[i], splat2(wv[i]), splat2(sv[i]));
         }
         if (c < cend) store_bf16<EL>(yrow + 2 * static_cast<int64_t>(c) * EL, acc);
       }
@@ -291,11 +338,12 @@ cudaError_t launch_combine_t(CombineArgs a, int sms, int* cache, cudaStream_t s)
 
 template <int FMT>
 cudaError_t launch_combine_fmt(const CombineArgs& a, int sms, cudaStream_t s) {
-  // 16 loads in flight per lane once a row is long enough to keep them busy
-  // (8 for int4, whose 32-element chunks need twice the accumulators)
-  const bool deep = FMT != kFmtInt4 && a.H / Chunk<FMT>::kElems >= 64;
-  return deep ? launch_combine_t<FMT, 16>(a, sms, g_occ_combine[2 * FMT], s)
-              : launch_combine_t<FMT, 8>(a, sms, g_occ_combine[2 * FMT + 1], s);
+  // bf16: 16 loads in flight per lane once a row is long enough to keep them
+  // busy; coded rows: 8 (see combine_kernel)
+  if constexpr (FMT == kFmtBf16) {
+    if (a.H / Chunk<FMT>::kElems >= 64) return launch_combine_t<FMT, 16>(a, sms, g_occ_combine[2 * FMT], s);
+  }
+  return launch_combine_t<FMT, 8>(a, sms, g_occ_combine[2 * FMT + 1], s);
 }
 
 }  // namespace

@@ -241,10 +241,14 @@ ep_status_t ep_route_dispatch(const ep_config_t* cfg, const float* logits, const
   r.tile_counts = a.tile_counts;
   r.lrank = a.lrank;
   r.ticket = a.ticket;
-  if (ep::small_batch(r.T, r.E, r.tile)) {  // one CTA routes and lays out the batch, then the scatter
-    if (ep::launch_route_layout_small(r, a, stream) != cudaSuccess) return EP_ERR_CUDA;
-    a.pairs_early = 0;  // the routing kernel just before wrote topk_idx and lrank
-    return from_cuda(ep::launch_scatter(a, sms, stream));
+  if (ep::small_batch(r.T, r.E, r.tile)) {  // one cluster routes and lays out the batch, then the scatter
+    const cudaError_t e = ep::launch_route_layout_small(r, a, stream);
+    if (e == cudaSuccess) {
+      a.pairs_early = 0;  // the routing kernel just before wrote topk_idx and lrank
+      return from_cuda(ep::launch_scatter(a, sms, stream));
+    }
+    if (e != cudaErrorNotSupported) return EP_ERR_CUDA;
+    // the cluster cannot be resident on this device: the general path below
   }
   const cudaError_t err = ep::launch_route_count(r, stream);
   if (err != cudaSuccess) return EP_ERR_CUDA;

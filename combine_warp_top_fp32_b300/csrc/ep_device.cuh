@@ -389,9 +389,15 @@ __device__ __forceinline__ float absmax_bf16x8(uint4 a) {
   return m;
 }
 
-// Signed int8 byte i of a word, widened exactly to float.
-__device__ __forceinline__ float i8_at(uint32_t w, int i) {
-  return static_cast<float>(static_cast<int8_t>((w >> (8 * i)) & 0xffu));
+// The four signed int8 codes of a word, widened exactly to float without the
+// conversion unit: with its sign bit flipped, byte i is q + 128, which one
+// byte permute places as the low mantissa byte of 2^23 (0x4B000000), giving
+// the float 2^23 + 128 + q; subtracting 2^23 + 128 leaves q exactly.
+__device__ __forceinline__ void i8x4_to_f32(uint32_t w, float (&f)[4]) {
+  const uint32_t b = w ^ 0x80808080u;
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+    f[i] = __fsub_rn(__uint_as_float(__byte_perm(b, 0x4B000000u, 0x7440u | static_cast<unsigned>(i))), 8388736.0f);
 }
 
 }  // namespace ep

@@ -134,8 +134,9 @@ cudaError_t launch_route_count(const RouteCountArgs& r, cudaStream_t s);
 // Small batches (at most kClusterTiles tiles of 32 tokens, E <= 256): one
 // thread-block cluster of one CTA per tile routes the batch and forms the
 // whole layout (topk_idx / topk_w, lrank, tile_base and every layout output)
-// in one launch; the scatter follows. Returns cudaErrorNotSupported when the
-// batch is not small.
+// in one launch; the scatter follows. Returns cudaErrorNotSupported, having
+// launched nothing, when the batch is not small or such a cluster cannot be
+// resident on the device.
 constexpr int kClusterTiles = 8;      // the portable cluster size
 constexpr int kClusterExperts = 256;  // experts per routing lane group of 32: at most 8 values per lane
 bool small_batch(int T, int E, int tile);

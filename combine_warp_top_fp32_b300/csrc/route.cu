@@ -664,6 +664,28 @@ cudaError_t launch_route_layout_cluster_t(const RouteCountArgs& r, const Dispatc
   attr[1].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
+  // Whether a cluster of C such CTAs can be resident at all (it may not be,
+  // e.g. when the process is limited to a share of the SMs): asked once per
+  // device and cluster size; if not, the caller takes the general path.
+  static signed char fits[64][kClusterTiles + 1];  // 0 unknown, 1 yes, -1 no
+  int dev = 0;
+  cudaError_t err = cudaGetDevice(&dev);
+  if (err != cudaSuccess) return err;
+  signed char f = dev < 64 ? fits[dev][C] : 0;
+  if (f == 0) {
+    cudaLaunchConfig_t q = cfg;  // the cluster shape alone
+    q.attrs = attr + 1;
+    q.numAttrs = 1;
+    int clusters = 0;
+    err = cudaOccupancyMaxActiveClusters(&clusters, route_layout_cluster_kernel<VPL, VEC4>, &q);
+    if (err != cudaSuccess) {
+      (void)cudaGetLastError();  // a refused query is not an error of this call
+      clusters = 0;
+    }
+    f = clusters > 0 ? 1 : -1;
+    if (dev < 64) fits[dev][C] = f;
+  }
+  if (f < 0) return cudaErrorNotSupported;
   return cudaLaunchKernelEx(&cfg, route_layout_cluster_kernel<VPL, VEC4>, r.logits, r.T, r.E, r.k, lanes_log2,
                             r.renorm, a.R, a.cap, r.topk_idx, r.topk_w, a.lrank, a.tile_base, a.expert_counts,
                             a.expert_raw, a.expert_off, a.rank_off, a.n_dropped);

@@ -275,7 +275,9 @@ ep_status_t ep_dispatch_static(const ep_config_t* cfg, const void* x, const int3
  *                                  (q the int8, E4M3 or int4 code, widened
  *                                  exactly)
  *   ws, ws_bytes workspace (its status word records bad slot_row entries)
- * A token whose k slots were all dropped gets y = 0.
+ * A token whose k slots were all dropped gets y = 0. The E4M3 NaN codes (0x7F,
+ * 0xFF), which no encoder of this library writes, are outside the contract
+ * (they read as +-480).
  */
 ep_status_t ep_combine(const ep_config_t* cfg, const void* expert_out, const float* out_scales,
                        int32_t out_payload, const int32_t* slot_row, const float* topk_w, void* y,

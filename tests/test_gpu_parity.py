@@ -300,6 +300,37 @@ def test_coded_return_path(ep, orc, shape, fmt):
     np.testing.assert_array_equal(_bits(y), y_orc)
 
 
+@pytest.mark.parametrize("fmt", ["int8", "fp8", "int4"])
+def test_combine_decodes_every_code(ep, orc, fmt):
+    """Every code value (256 int8 bytes, 254 non-NaN E4M3 bytes, 16 nibbles in
+    every position) widened by the combine and summed over two slots, against
+    the oracle's combine on the same codes, bit for bit. Scales span normal,
+    tiny (subnormal products) and large values."""
+    T, k, E = 8, 2, 8
+    int4 = fmt == "int4"
+    H = 512 if int4 else 256
+    kind = {"int8": ep.EP_PAYLOAD_INT8, "fp8": ep.EP_PAYLOAD_FP8, "int4": ep.EP_PAYLOAD_INT4}[fmt]
+    rng = np.random.default_rng(17)
+    rows = T * k
+    codes = np.stack([rng.permutation(256) for _ in range(rows)]).astype(np.uint8)  # every byte in every row
+    if fmt == "fp8":
+        codes[(codes & 0x7F) == 0x7F] ^= 1  # E4M3 NaN codes are never written: 0x7F -> 0x7E, 0xFF -> 0xFE
+    q_np = codes.view(np.int8) if fmt == "int8" else codes
+    s_np = np.array([1.0, 0.37, 3.1e-3, 2.0 ** -120, 1.0e-38, 5.5e3, 0.0, 1.7e30] * 2, np.float32)
+    w_np = rng.uniform(0.05, 1.0, (T, k)).astype(np.float32)
+    slot_row = rng.permutation(rows).astype(np.int32).reshape(T, k)
+    slot_row[3, 1] = -1  # a dropped slot
+    y_orc = orc.combine(q_np, s_np, slot_row, w_np, T, k, int4=int4)
+    cfg = ep.make_config(T, H, E, k, 1, payload=kind)
+    buf = ep.EpBuffers.allocate(cfg)
+    y = torch.empty(T, H, dtype=torch.bfloat16, device="cuda")
+    ep.ep_combine(cfg, torch.from_numpy(q_np).cuda(), torch.from_numpy(s_np).cuda(), kind,
+                  torch.from_numpy(slot_row).cuda(), torch.from_numpy(w_np).cuda(), y, buf.ws)
+    torch.cuda.synchronize()
+    assert ep.ep_get_error(buf.ws) == ep.EP_OK
+    np.testing.assert_array_equal(_bits(y), y_orc)
+
+
 @pytest.mark.parametrize("payload", [0, 1, 2, 3])
 def test_identity_experts_round_trip(ep, payload):
     """combine(dispatch(x)) with identity experts and renormalised weights gives x back."""
