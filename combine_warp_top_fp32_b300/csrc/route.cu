@@ -22,6 +22,7 @@
 //     compensated (TwoSum) arithmetic; each chosen expert's numerator uses
 //     expf, so the weight stays within 1e-6 of the exact value.
 #include "ep_internal.h"
+#include "layout.cuh"
 
 namespace ep {
 namespace {
@@ -563,7 +564,6 @@ __global__ void __launch_bounds__(1024, 1) route_layout_cluster_kernel(
   int* counts_s = reinterpret_cast<int*>(smem + E);    // [E][C] (CTA 0) every tile's count per expert
   int* kept_s = counts_s + E * C;                      // [E] (CTA 0)
   int* drop_s = kept_s + E;                            // [E] (CTA 0)
-  const int lane = threadIdx.x & 31;
   const int warp = threadIdx.x >> 5;
   const int b = blockIdx.x;
   const int64_t t0 = static_cast<int64_t>(b) * 32;
@@ -616,32 +616,7 @@ __global__ void __launch_bounds__(1024, 1) route_layout_cluster_kernel(
   __syncthreads();
   if (warp != 0) return;
 
-  // expert and rank offsets, one warp: lane l sums experts [l*per, (l+1)*per)
-  const int G = E / R;  // rank r starts at its first expert r*G
-  const int per = (E + 31) / 32;
-  const int e0 = lane * per;
-  int kv = 0, dv = 0;
-  for (int j = 0; j < per; ++j)
-    if (e0 + j < E) {
-      kv += kept_s[e0 + j];
-      dv += drop_s[e0 + j];
-    }
-  const int ki = warp_inclusive_scan(kv);
-  const int di = warp_inclusive_scan(dv);
-  int run = ki - kv;
-  for (int j = 0; j < per; ++j) {
-    const int e = e0 + j;
-    if (e < E) {
-      expert_off[e] = run;
-      if (e % G == 0) rank_off[e / G] = run;
-      run += kept_s[e];
-    }
-  }
-  if (lane == 31) {
-    expert_off[E] = ki;
-    rank_off[R] = ki;
-    *n_dropped = di;
-  }
+  expert_offsets_warp(kept_s, drop_s, E, R, expert_off, rank_off, n_dropped);
 }
 
 template <int VPL, bool VEC4>
