@@ -21,6 +21,13 @@
 //     error carried into the exponential (exp_shifted_term), summed with
 //     compensated (TwoSum) arithmetic; each chosen expert's numerator uses
 //     expf, so the weight stays within 1e-6 of the exact value.
+//
+// Kernels: route_topk_kernel (ep_route: routing alone, a grid-stride loop
+// over tokens); route_count_kernel (ep_route_dispatch: one CTA per tile of
+// tokens routes the tile and writes its per-expert counts and in-tile ranks,
+// the dispatch's count step); route_layout_cluster_kernel (ep_route_dispatch
+// on batches of at most eight 32-token tiles: one thread-block cluster routes
+// the batch and forms the whole layout, the count and scan steps together).
 #include "ep_internal.h"
 #include "layout.cuh"
 
