@@ -181,7 +181,10 @@ ep_status_t ep_dispatch(const ep_config_t* cfg, const void* x, const int32_t* to
  * would write; the arguments mean what they mean there (logits [T, E] fp32
  * in, 16-byte aligned; topk_idx / topk_w [T, k] out). One kernel fewer runs:
  * a CTA routes one tile of tokens and counts its per-expert copies in shared
- * memory, then the scan and the scatter run as in ep_dispatch.
+ * memory, then the scan and the scatter run as in ep_dispatch. A batch of at
+ * most 256 tokens with E <= 256 takes two kernels: one thread-block cluster
+ * routes it and forms the whole layout, then the scatter (where such a
+ * cluster cannot be resident, the three-kernel form runs instead).
  */
 ep_status_t ep_route_dispatch(const ep_config_t* cfg, const float* logits, const void* x, int32_t* topk_idx,
                               float* topk_w, void* payload, float* scales, int32_t* row_slot, int32_t* slot_row,
