@@ -1,0 +1,50 @@
+"""The bench's JSON line on a small workload (GPU): every key the line
+promises, with values consistent with each other and with the workload."""
+import io
+import json
+from contextlib import redirect_stdout
+
+import pytest
+import torch
+
+pytestmark = pytest.mark.gpu
+
+
+def test_bench_line_on_decode_latency(monkeypatch):
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA GPU")
+    import bench
+    from combine_warp_top_fp32_b300 import workloads
+
+    monkeypatch.delenv("RANK", raising=False)
+    monkeypatch.delenv("WORLD_SIZE", raising=False)
+    steps = 3
+    buf = io.StringIO()
+    with redirect_stdout(buf):
+        rc = bench.main(["--workload", "decode-latency", "--steps", str(steps), "--warmup", "3",
+                         "--no-cpu-baseline", "--e2e-steps", "3"])
+    assert rc == 0
+    lines = [ln for ln in buf.getvalue().splitlines() if ln.startswith("{")]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    w = workloads.WORKLOADS["decode-latency"]
+
+    assert d["unit"] == "tokens/s" and d["higher_is_better"] is True and d["n_gpus"] == 1
+    assert d["value"] > 0
+    assert d["value"] == pytest.approx(w.T / (d["ms_per_step"] / 1e3), rel=1e-6)
+    # the batch is laid out by one cluster launch: route+layout, scatter, combine
+    assert d["gpu_launches"] == 3 * steps
+    assert d["config"]["workload"] == "decode-latency" and d["config"]["payload"] == "int8"
+
+    roof = d["roofline"]
+    assert roof["bound"] == "hbm" and roof["unit"] == "GB/s" and roof["peak"] > 0
+    assert roof["frac"] == pytest.approx(roof["achieved"] / roof["peak"])
+
+    e2e = d["e2e"]
+    assert e2e["value"] > 0 and e2e["unit"] == "tokens/s"
+    assert e2e["h2d_bytes_per_step"] == w.T * w.E * 4 + w.T * w.H * 2  # logits + x
+    assert e2e["d2h_bytes_per_step"] == w.T * w.H * 2  # y
+
+    both = d["int8_both_directions"]
+    assert both["value"] > 0 and both["bytes_per_step"] < d["hbm"]["bytes_per_step"]
+    assert {"sm_mhz", "sm_max_mhz", "reasons"} <= set(d["clocks"])
