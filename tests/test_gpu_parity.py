@@ -210,6 +210,8 @@ EDGE = [
     (100, 32, 160, 5, 8, 0.3, 0, 0, "cluster layout, 5 values per lane, ragged tile, drops"),
     (250, 64, 64, 6, 8, 0.0, 2, 0, "cluster layout, two tokens per warp in flight"),
     (33, 48, 3, 3, 3, 0.0, 1, 1, "cluster layout of two tiles, one token in the second"),
+    (200, 32, 64, 32, 4, 0.5, 1, 1, "cluster layout at the maximum k = 32, drops"),
+    (160, 64, 256, 1, 256, 0.0, 3, 0, "cluster layout, k = 1, one expert per rank, int4"),
 ]
 
 
