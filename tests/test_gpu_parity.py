@@ -302,6 +302,30 @@ def test_coded_return_path(ep, orc, shape, fmt):
     np.testing.assert_array_equal(_bits(y), y_orc)
 
 
+def test_combine_slot_order_and_fma(ep, orc):
+    """The two combine pins of the oracle on the GPU: token 0 sums 2^24, 1,
+    -2^24 in slot order (0 in fp32 with ties to even, 1 in any other order);
+    token 1 adds w1*v1 to -fl(w1*v1), which only a fused multiply-add leaves
+    as the nonzero residual."""
+    H, k, T = 16, 3, 2
+    w1 = np.float32(1.0 + 2.0**-20 + 2.0**-23)
+    v1 = np.float32(1.0 + 2.0**-7)
+    P = np.float32(w1 * v1)
+    vals = np.array([2.0**24, 1.0, -(2.0**24), -1.0, v1], np.float32)
+    eo = (np.repeat(vals[:, None], H, axis=1).view(np.uint32) >> 16).astype(np.uint16)  # exact in bf16
+    slot_row = np.array([0, 1, 2, 3, 4, -1], np.int32)
+    w = np.array([1.0, 1.0, 1.0, P, w1, 0.5], np.float32)
+    y_orc = orc.combine(eo, None, slot_row, w, T, k)
+    cfg = ep.make_config(T, H, 8, k, 1)
+    buf = ep.EpBuffers.allocate(cfg)
+    y = torch.empty(T, H, dtype=torch.bfloat16, device="cuda")
+    ep.ep_combine(cfg, torch.from_numpy(eo.view(np.int16)).cuda().view(torch.bfloat16), None, ep.EP_PAYLOAD_BF16,
+                  torch.from_numpy(slot_row).cuda(), torch.from_numpy(w).cuda(), y, buf.ws)
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(_bits(y), y_orc)
+    assert np.all(bf16_to_f32(y_orc[0]) == 0.0) and np.all(bf16_to_f32(y_orc[1]) != 0.0)
+
+
 @pytest.mark.parametrize("fmt", ["int8", "fp8", "int4"])
 def test_combine_decodes_every_code(ep, orc, fmt):
     """Every code value (256 int8 bytes, 254 non-NaN E4M3 bytes, 16 nibbles in

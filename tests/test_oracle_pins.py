@@ -418,6 +418,34 @@ def test_combine_exact_small_sums(orc):
     assert np.all(_bf16_bits_to_f32(y) == 0.25 * (-8.0) + 1.0 * 5.0)
 
 
+def test_combine_follows_slot_order(orc):
+    # slot order is part of the definition: 2^24 + 1 rounds back to 2^24 in
+    # fp32 (ties to even), so 2^24, 1, -2^24 in slot order sum to 0, while any
+    # order that adds -2^24 before 1 would give 1
+    H = 8
+    eo = np.stack([_f32_bits_to_bf16_bits(np.full(H, v, np.float32)) for v in (2.0**24, 1.0, -(2.0**24))])
+    y = orc.combine(eo, None, np.array([0, 1, 2], np.int32), np.ones(3, np.float32), 1, 3)
+    assert np.all(_bf16_bits_to_f32(y) == 0.0)
+    y = orc.combine(eo, None, np.array([2, 1, 0], np.int32), np.ones(3, np.float32), 1, 3)
+    assert np.all(_bf16_bits_to_f32(y) == 1.0)
+
+
+def test_combine_uses_fused_multiply_add(orc):
+    # slot 0 puts acc = -P with P = fl(w1 * v1); slot 1 adds w1 * v1. With one
+    # rounding per fma the result is the exact residual w1*v1 - P = 2^-27 +
+    # 2^-30 (exact in bf16); a separate multiply and add would give 0.
+    H = 8
+    w1 = np.float32(1.0 + 2.0**-20 + 2.0**-23)
+    v1 = np.float32(1.0 + 2.0**-7)
+    P = np.float32(w1 * v1)
+    residual = float(w1) * float(v1) - float(P)
+    assert residual == 2.0**-27 + 2.0**-30
+    eo = np.stack([_f32_bits_to_bf16_bits(np.full(H, -1.0, np.float32)),
+                   _f32_bits_to_bf16_bits(np.full(H, v1, np.float32))])
+    y = orc.combine(eo, None, np.array([0, 1], np.int32), np.array([P, w1], np.float32), 1, 2)
+    assert np.all(_bf16_bits_to_f32(y) == np.float32(residual))
+
+
 def test_combine_tokens_matches_full_combine(orc):
     rng = np.random.default_rng(12)
     T, H, k, N = 20, 32, 3, 50
