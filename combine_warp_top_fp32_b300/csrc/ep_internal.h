@@ -83,6 +83,51 @@ inline cudaError_t launch_pdl(void (*kernel)(KArgs...), int grid, int block, siz
   return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 
+// One thread-block cluster of `grid` CTAs (1..kMaxCluster) launched like
+// launch_pdl. Whether such a cluster can be resident at all (it may not be,
+// e.g. when the process is limited to a share of the SMs) is asked once per
+// device and cluster size and kept in `fits` (0 unknown, 1 yes, -1 no); if it
+// cannot, nothing is launched and cudaErrorNotSupported is returned, so that
+// the caller can take its general path.
+constexpr int kMaxCluster = 8;  // the portable cluster size
+using ClusterFits = signed char[64][kMaxCluster + 1];
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_cluster_pdl(void (*kernel)(KArgs...), int grid, int block, size_t smem, cudaStream_t s,
+                                      ClusterFits& fits, Args&&... args) {
+  if (grid < 1 || grid > kMaxCluster) return cudaErrorNotSupported;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(grid));
+  cfg.blockDim = dim3(static_cast<unsigned>(block));
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = static_cast<unsigned>(grid);
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  int dev = 0;
+  cudaError_t err = cudaGetDevice(&dev);
+  if (err != cudaSuccess) return err;
+  signed char f = dev < 64 ? fits[dev][grid] : 0;
+  if (f == 0) {
+    cfg.numAttrs = 1;  // the cluster shape alone
+    int clusters = 0;
+    err = cudaOccupancyMaxActiveClusters(&clusters, kernel, &cfg);
+    if (err != cudaSuccess) {
+      (void)cudaGetLastError();  // a refused query is not an error of this call
+      clusters = 0;
+    }
+    f = clusters > 0 ? 1 : -1;
+    if (dev < 64) fits[dev][grid] = f;
+  }
+  if (f < 0) return cudaErrorNotSupported;
+  cfg.numAttrs = 2;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
 cudaError_t launch_route(const float* logits, int T, int E, int k, int renorm, int32_t* idx, float* w, int sms,
                          cudaStream_t s);
 
@@ -137,7 +182,7 @@ cudaError_t launch_route_count(const RouteCountArgs& r, cudaStream_t s);
 // in one launch; the scatter follows. Returns cudaErrorNotSupported, having
 // launched nothing, when the batch is not small or such a cluster cannot be
 // resident on the device.
-constexpr int kClusterTiles = 8;      // the portable cluster size
+constexpr int kClusterTiles = kMaxCluster;
 constexpr int kClusterExperts = 256;  // experts per routing lane group of 32: at most 8 values per lane
 bool small_batch(int T, int E, int tile);
 cudaError_t launch_route_layout_small(const RouteCountArgs& r, const DispatchArgs& a, cudaStream_t s);

@@ -1,5 +1,6 @@
-// layout.cuh — the last step of the dispatch layout for a kernel that forms
-// it within one CTA (the small-batch cluster kernel).
+// layout.cuh — pieces for a kernel that finishes the dispatch layout inside
+// one thread-block cluster (the small-batch route+layout kernel): barriers and
+// stores across the cluster's shared memory, and the expert / rank offsets.
 //
 // From each expert's kept and dropped counts (cap already applied):
 //   expert_off[e] = sum of kept counts of the experts before e  (E+1 entries),
@@ -13,6 +14,26 @@
 #include "ep_device.cuh"
 
 namespace ep {
+
+// Thread-block cluster helpers (distributed shared memory). Every thread of
+// every CTA of the cluster must reach each barrier (the .aligned forms).
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.aligned;" ::: "memory"); }
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// Address of `p` (this CTA's shared memory) in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t cluster_map(const void* p, uint32_t rank) {
+  const uint32_t local = static_cast<uint32_t>(__cvta_generic_to_shared(p));
+  uint32_t remote;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(local), "r"(rank));
+  return remote;
+}
+__device__ __forceinline__ void st_cluster_u32(uint32_t addr, uint32_t v) {
+  asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
 
 // One warp (all 32 lanes call it): lane l sums experts [l*per, (l+1)*per),
 // per = ceil(E/32), then a warp scan gives every expert's offset.

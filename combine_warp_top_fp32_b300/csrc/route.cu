@@ -532,25 +532,6 @@ __global__ void __launch_bounds__(VPL >= 16 ? 256 : 512) route_count_kernel(
   }
 }
 
-// ---- thread-block cluster helpers (distributed shared memory) ----
-__device__ __forceinline__ void cluster_arrive_relaxed() {
-  asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
-}
-__device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.aligned;" ::: "memory"); }
-__device__ __forceinline__ void cluster_sync() {
-  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-// Address of `p` (this CTA's shared memory) in CTA `rank` of the cluster.
-__device__ __forceinline__ uint32_t cluster_map(const void* p, uint32_t rank) {
-  const uint32_t local = static_cast<uint32_t>(__cvta_generic_to_shared(p));
-  uint32_t remote;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(local), "r"(rank));
-  return remote;
-}
-__device__ __forceinline__ void st_cluster_u32(uint32_t addr, uint32_t v) {
-  asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
-}
-
 // Small batches (at most kClusterTiles tiles of 32 tokens): one cluster of
 // one CTA per tile, a warp per token. Each CTA routes its tile and ranks its
 // pairs as route_count_kernel does, but pushes its per-expert tile counts
@@ -632,45 +613,10 @@ cudaError_t launch_route_layout_cluster_t(const RouteCountArgs& r, const Dispatc
   constexpr int kBlock = 1024;  // a warp per token of the tile
   const int C = (r.T + 31) / 32;
   const int smem = (r.E + r.E * C + 2 * r.E) * static_cast<int>(sizeof(uint32_t));  // <= 11 KB
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>(C));
-  cfg.blockDim = dim3(kBlock);
-  cfg.dynamicSmemBytes = static_cast<size_t>(smem);
-  cfg.stream = s;
-  cudaLaunchAttribute attr[2];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  attr[1].id = cudaLaunchAttributeClusterDimension;
-  attr[1].val.clusterDim.x = static_cast<unsigned>(C);
-  attr[1].val.clusterDim.y = 1;
-  attr[1].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 2;
-  // Whether a cluster of C such CTAs can be resident at all (it may not be,
-  // e.g. when the process is limited to a share of the SMs): asked once per
-  // device and cluster size; if not, the caller takes the general path.
-  static signed char fits[64][kClusterTiles + 1];  // 0 unknown, 1 yes, -1 no
-  int dev = 0;
-  cudaError_t err = cudaGetDevice(&dev);
-  if (err != cudaSuccess) return err;
-  signed char f = dev < 64 ? fits[dev][C] : 0;
-  if (f == 0) {
-    cudaLaunchConfig_t q = cfg;  // the cluster shape alone
-    q.attrs = attr + 1;
-    q.numAttrs = 1;
-    int clusters = 0;
-    err = cudaOccupancyMaxActiveClusters(&clusters, route_layout_cluster_kernel<VPL, VEC4>, &q);
-    if (err != cudaSuccess) {
-      (void)cudaGetLastError();  // a refused query is not an error of this call
-      clusters = 0;
-    }
-    f = clusters > 0 ? 1 : -1;
-    if (dev < 64) fits[dev][C] = f;
-  }
-  if (f < 0) return cudaErrorNotSupported;
-  return cudaLaunchKernelEx(&cfg, route_layout_cluster_kernel<VPL, VEC4>, r.logits, r.T, r.E, r.k, lanes_log2,
-                            r.renorm, a.R, a.cap, r.topk_idx, r.topk_w, a.lrank, a.tile_base, a.expert_counts,
-                            a.expert_raw, a.expert_off, a.rank_off, a.n_dropped);
+  static ClusterFits fits;
+  return launch_cluster_pdl(route_layout_cluster_kernel<VPL, VEC4>, C, kBlock, static_cast<size_t>(smem), s, fits,
+                            r.logits, r.T, r.E, r.k, lanes_log2, r.renorm, a.R, a.cap, r.topk_idx, r.topk_w, a.lrank,
+                            a.tile_base, a.expert_counts, a.expert_raw, a.expert_off, a.rank_off, a.n_dropped);
 }
 
 template <int VPL, bool VEC4>
