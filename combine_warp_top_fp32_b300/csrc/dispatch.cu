@@ -437,10 +437,10 @@ cudaError_t launch_count(const DispatchArgs& a, const Pairs& src, cudaStream_t s
     int dev = 0;
     cudaError_t err = cudaGetDevice(&dev);
     if (err != cudaSuccess) return err;
-    if (dev >= 64 || smem_set[dev] < smem) {
+    if (dev >= 64 || cache_load(&smem_set[dev]) < smem) {
       err = cudaFuncSetAttribute(count_kernel<Pairs>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
       if (err != cudaSuccess) return err;
-      if (dev < 64) smem_set[dev] = smem;
+      if (dev < 64) cache_store(&smem_set[dev], smem);
     }
   }
   int cblock = ((a.tile * a.k + 31) / 32) * 32;

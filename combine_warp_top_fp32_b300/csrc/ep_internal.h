@@ -49,6 +49,19 @@ inline WsLayout ws_layout(int T, int E, int k) {
   return L;
 }
 
+// Per-device caches of launch facts (occupancy, attributes already set,
+// cluster residency) are shared by every host thread that calls the library;
+// they are read and written with relaxed atomics, so concurrent first calls
+// at worst repeat a query.
+template <typename T>
+inline T cache_load(const T* p) {
+  return __atomic_load_n(p, __ATOMIC_RELAXED);
+}
+template <typename T>
+inline void cache_store(T* p, T v) {
+  __atomic_store_n(p, v, __ATOMIC_RELAXED);
+}
+
 // CTAs of `kernel` (at `block` threads, `smem` dynamic shared bytes) that fit
 // on one SM at once, cached per device in cache[64]; 1 if the query fails. A
 // grid-stride kernel launched with sms * this many CTAs runs in one wave: a
@@ -58,10 +71,13 @@ template <typename K>
 inline int resident_ctas(K kernel, int block, int smem, int* cache) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return 1;
-  if (dev < 64 && cache[dev] > 0) return cache[dev];
+  if (dev < 64) {
+    const int c = cache_load(&cache[dev]);
+    if (c > 0) return c;
+  }
   int n = 0;
   if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, block, smem) != cudaSuccess || n < 1) n = 1;
-  if (dev < 64) cache[dev] = n;
+  if (dev < 64) cache_store(&cache[dev], n);
   return n;
 }
 
@@ -111,7 +127,7 @@ inline cudaError_t launch_cluster_pdl(void (*kernel)(KArgs...), int grid, int bl
   int dev = 0;
   cudaError_t err = cudaGetDevice(&dev);
   if (err != cudaSuccess) return err;
-  signed char f = dev < 64 ? fits[dev][grid] : 0;
+  signed char f = dev < 64 ? cache_load(&fits[dev][grid]) : static_cast<signed char>(0);
   if (f == 0) {
     cfg.numAttrs = 1;  // the cluster shape alone
     int clusters = 0;
@@ -121,7 +137,7 @@ inline cudaError_t launch_cluster_pdl(void (*kernel)(KArgs...), int grid, int bl
       clusters = 0;
     }
     f = clusters > 0 ? 1 : -1;
-    if (dev < 64) fits[dev][grid] = f;
+    if (dev < 64) cache_store(&fits[dev][grid], f);
   }
   if (f < 0) return cudaErrorNotSupported;
   cfg.numAttrs = 2;

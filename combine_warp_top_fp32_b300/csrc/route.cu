@@ -640,10 +640,10 @@ cudaError_t launch_route_count_t(const RouteCountArgs& r, int lanes_log2, cudaSt
     int dev = 0;
     cudaError_t err = cudaGetDevice(&dev);
     if (err != cudaSuccess) return err;
-    if (dev >= 64 || smem_set[dev] < smem) {
+    if (dev >= 64 || cache_load(&smem_set[dev]) < smem) {
       err = cudaFuncSetAttribute(route_count_kernel<VPL, VEC4>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
       if (err != cudaSuccess) return err;
-      if (dev < 64) smem_set[dev] = smem;
+      if (dev < 64) cache_store(&smem_set[dev], smem);
     }
   }
   return launch_pdl(route_count_kernel<VPL, VEC4>, r.ntiles > 0 ? r.ntiles : 1, kBlock, static_cast<size_t>(smem),
