@@ -313,11 +313,10 @@ def run_gpu(args):
     assert ep.ep_get_error(buf.ws) == ep.EP_OK
     N = int(buf.rank_off[-1].item())
     if args.path == "fused":
-        # ep_route_dispatch (route+count, scan, scatter) then ep_combine; a
-        # batch of at most eight 32-token tiles with E <= 256 is routed and
-        # laid out by one cluster launch (route+layout, scatter, combine)
-        small = 0 < w.T <= 8 * 32 and w.E <= 256
-        launches_per_step = (3 if small else 4) if w.T > 0 else 2
+        # ep_route_dispatch (as many kernels as the library reports for this
+        # shape and device: one cooperative launch, or the cluster form, or
+        # route+count, scan, scatter), then ep_combine (none for an empty batch)
+        launches_per_step = ep.ep_route_dispatch_kernels(cfg) + (1 if w.T > 0 else 0)
     else:
         # ep_route; ep_dispatch (count, scan, scatter); ep_combine
         launches_per_step = 5 if w.T > 0 else 2
@@ -404,7 +403,8 @@ def run_gpu(args):
     stage_gbs = {s: nb[s] / (stage_ms[s] / 1e3) / 1e9 for s in stage_ms}
     dominant = max(stage_ms, key=stage_ms.get)
     kernel_names = {"route": "route_topk_kernel", "dispatch": "count+scan+scatter_kernel",
-                    "route+dispatch": "route_count+scan+scatter_kernel",
+                    "route+dispatch": ("route_dispatch_fused_kernel" if ep.ep_route_dispatch_kernels(cfg) == 1
+                                       else "route_count+scan+scatter_kernel"),
                     "combine": "combine_kernel<bf16>"}
     traffic = recorded_traffic(dominant, w.name, args.payload)
 

@@ -34,7 +34,7 @@ EXPORTS = (
     "ep_status_string", "ep_config_check", "ep_capacity", "ep_max_rows", "ep_workspace_size",
     "ep_workspace_init", "ep_route", "ep_dispatch", "ep_combine", "ep_quantize_rows", "ep_get_error",
     "ep_load_stats", "ep_dispatch_static", "ep_route_dispatch", "ep_quantize_rows_fp8", "ep_bitmap_encode",
-    "ep_bitmap_layout", "ep_quantize_rows_int4",
+    "ep_bitmap_layout", "ep_quantize_rows_int4", "ep_debug_set", "ep_route_dispatch_kernels",
 )
 
 
@@ -86,6 +86,8 @@ def _load():
     lib.ep_load_stats.argtypes = [P, I32, ctypes.POINTER(ep_load_stats_t)]
     lib.ep_dispatch_static.argtypes = [CFG, P, P, P, P, P, P, P, P, P, P, P, P]
     lib.ep_route_dispatch.argtypes = [CFG, P, P, P, P, P, P, P, P, P, P, P, P, P, P, SZ, P]
+    lib.ep_debug_set.argtypes = [I32, I32]
+    lib.ep_route_dispatch_kernels.argtypes = [CFG, ctypes.POINTER(I32)]
     for name in EXPORTS:
         if name not in ("ep_status_string", "ep_max_rows"):
             getattr(lib, name).restype = ctypes.c_int
@@ -166,6 +168,13 @@ def ep_capacity(cfg: ep_config_t) -> int:
 
 def ep_max_rows(cfg: ep_config_t) -> int:
     return int(lib.ep_max_rows(ctypes.byref(cfg)))
+
+
+def ep_route_dispatch_kernels(cfg: ep_config_t) -> int:
+    """Kernels ep_route_dispatch launches for cfg on the current device."""
+    n = ctypes.c_int32()
+    _check(lib.ep_route_dispatch_kernels(ctypes.byref(cfg), ctypes.byref(n)), "ep_route_dispatch_kernels")
+    return n.value
 
 
 def ep_workspace_size(cfg: ep_config_t) -> int:
@@ -269,6 +278,17 @@ def ep_quantize_rows_int4(inp, q, scales, stream=None):
     n, H = inp.shape
     _check(lib.ep_quantize_rows_int4(_ptr(inp, torch.bfloat16, "in"), int(n), int(H), _ptr(q, torch.uint8, "q"),
                                      _ptr(scales, torch.float32, "scales"), _stream(stream)), "ep_quantize_rows_int4")
+
+
+EP_DEBUG_FORCE_WAIT_TIMEOUT = 1
+EP_DEBUG_ROUTE_DISPATCH_FORM = 2
+EP_FORM_AUTO, EP_FORM_SINGLE, EP_FORM_CHAIN = 0, 1, 2
+
+
+def ep_debug_set(option: int, value: int):
+    """Process-wide test hooks (include/ep.h): force the single-launch form's
+    device-wide wait to time out, or choose the form of ep_route_dispatch."""
+    _check(lib.ep_debug_set(int(option), int(value)), "ep_debug_set")
 
 
 def ep_get_error(ws, stream=None) -> int:

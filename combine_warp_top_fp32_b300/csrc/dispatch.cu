@@ -230,16 +230,17 @@ __device__ __forceinline__ int gather_rows(unsigned& mask, int row, char* base, 
 }
 
 // 32 bytes (16 bf16) of x per thread: one 32-byte load when the row base is
-// 32-byte aligned (V8), else two 16-byte loads.
+// 32-byte aligned (V8), else two 16-byte loads; either way the lines read
+// become the first to leave L2 (pol: an evict-first policy).
 template <bool V8>
-__device__ __forceinline__ void ld_x32(const char* p, uint4& lo, uint4& hi) {
+__device__ __forceinline__ void ld_x32(const char* p, uint4& lo, uint4& hi, uint64_t pol) {
   if constexpr (V8) {
-    asm volatile("ld.global.nc.L1::no_allocate.v8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+    asm volatile("ld.global.nc.L1::no_allocate.L2::evict_first.v8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
                  : "=r"(lo.x), "=r"(lo.y), "=r"(lo.z), "=r"(lo.w), "=r"(hi.x), "=r"(hi.y), "=r"(hi.z), "=r"(hi.w)
                  : "l"(p));
   } else {
-    lo = ld_stream_v4(p);
-    hi = ld_stream_v4(p + 16);
+    lo = ld_stream_v4_hint(p, pol);
+    hi = ld_stream_v4_hint(p + 16, pol);
   }
 }
 
@@ -263,12 +264,13 @@ __global__ void __launch_bounds__(512) scatter_code_kernel(const DispatchArgs a,
   const int warp = c >> 5, lane = c & 31, nw = B >> 5;
   const char* xb = static_cast<const char*>(a.x);
   const int64_t GS = gridDim.x;
+  const uint64_t pol = l2_evict_first_policy();  // x and payload lines: first out of L2
   auto ld_tok = [&](int64_t t, uint4 (&v)[2 * G]) {
 #pragma unroll
     for (int g = 0; g < G; ++g) {
       const int grp = c + g * B;
       if (t < a.T && grp < ngroup)
-        ld_x32<V8>(xb + (t * a.H + 16 * grp) * 2, v[2 * g], v[2 * g + 1]);
+        ld_x32<V8>(xb + (t * a.H + 16 * grp) * 2, v[2 * g], v[2 * g + 1], pol);
       else
         v[2 * g] = v[2 * g + 1] = make_uint4(0, 0, 0, 0);
     }
@@ -324,13 +326,13 @@ __global__ void __launch_bounds__(512) scatter_code_kernel(const DispatchArgs a,
         const uint2 q = quant16_int4_coded(cur[2 * g], cur[2 * g + 1], scale, inv);
         for (int j = 0; j < a.k; ++j) {
           const int row = rows_s[buf][j];
-          if (row >= 0) st_v2(static_cast<char*>(a.payload) + static_cast<int64_t>(row) * (a.H / 2) + 8 * grp, q);
+          if (row >= 0) st_v2_hint(static_cast<char*>(a.payload) + static_cast<int64_t>(row) * (a.H / 2) + 8 * grp, q, pol);
         }
       } else {
         const uint4 q = quant16_fmt<FMT>(cur[2 * g], cur[2 * g + 1], scale, inv);
         for (int j = 0; j < a.k; ++j) {
           const int row = rows_s[buf][j];
-          if (row >= 0) st_v4(static_cast<int8_t*>(a.payload) + static_cast<int64_t>(row) * a.H + 16 * grp, q);
+          if (row >= 0) st_v4_hint(static_cast<int8_t*>(a.payload) + static_cast<int64_t>(row) * a.H + 16 * grp, q, pol);
         }
       }
     }
@@ -357,6 +359,7 @@ __global__ void __launch_bounds__(256) scatter_bf16_kernel(const DispatchArgs a,
   const int64_t row_bytes = 2 * static_cast<int64_t>(a.H);
   const int nchunk = a.H >> 3;  // 16-byte chunks (8 elements)
   char* const pbase = static_cast<char*>(a.payload);
+  const uint64_t pol = l2_evict_first_policy();  // x and payload lines: first out of L2
 
   PairA a0{-1, -1}, a1{-1, -1}, a_next2{-1, -1};
   if (!a.pairs_early) pdl_wait();
@@ -393,7 +396,7 @@ __global__ void __launch_bounds__(256) scatter_bf16_kernel(const DispatchArgs a,
 #pragma unroll
         for (int u = 0; u < U; ++u) {
           const int c = c0 + 32 * u;
-          v[u] = c < nchunk ? ld_stream_v4(xr + 16 * static_cast<int64_t>(c)) : make_uint4(0, 0, 0, 0);
+          v[u] = c < nchunk ? ld_stream_v4_hint(xr + 16 * static_cast<int64_t>(c), pol) : make_uint4(0, 0, 0, 0);
         }
 #pragma unroll
         for (int u = 0; u < U; ++u) {
@@ -401,7 +404,7 @@ __global__ void __launch_bounds__(256) scatter_bf16_kernel(const DispatchArgs a,
           if (c >= nchunk) break;
 #pragma unroll
           for (int i = 0; i < 8; ++i)
-            if (i < nk) st_v4(p[i] + 16 * static_cast<int64_t>(c), v[u]);
+            if (i < nk) st_v4_hint(p[i] + 16 * static_cast<int64_t>(c), v[u], pol);
         }
       }
     } else {
@@ -409,13 +412,13 @@ __global__ void __launch_bounds__(256) scatter_bf16_kernel(const DispatchArgs a,
       // is warp-uniform because the gathers shuffle across all lanes
       for (int c0 = 0; c0 < nchunk; c0 += 32) {
         const int c = c0 + lane;
-        const uint4 v = c < nchunk ? ld_stream_v4(xr + 16 * static_cast<int64_t>(c)) : make_uint4(0, 0, 0, 0);
+        const uint4 v = c < nchunk ? ld_stream_v4_hint(xr + 16 * static_cast<int64_t>(c), pol) : make_uint4(0, 0, 0, 0);
         unsigned msk = kept;
         while (msk) {
           const int n = gather_rows(msk, row, pbase, row_bytes, p);
 #pragma unroll
           for (int i = 0; i < 8; ++i)
-            if (i < n && c < nchunk) st_v4(p[i] + 16 * static_cast<int64_t>(c), v);
+            if (i < n && c < nchunk) st_v4_hint(p[i] + 16 * static_cast<int64_t>(c), v, pol);
         }
       }
     }
@@ -423,7 +426,6 @@ __global__ void __launch_bounds__(256) scatter_bf16_kernel(const DispatchArgs a,
 }
 
 int count_smem_bytes(int E, int tile) { return 2 * E * (tile / 32) * static_cast<int>(sizeof(uint32_t)); }
-
 
 }  // namespace
 

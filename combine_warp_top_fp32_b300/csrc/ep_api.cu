@@ -19,16 +19,23 @@ constexpr int kMaxDevices = 64;
 
 int g_sm_count[kMaxDevices];  // per-device SM count, filled on first use
 
-// SM count of the current device (cached); 0 on failure.
-int current_sm_count() {
+// A device attribute of the current device, cached per device (relaxed
+// atomics: concurrent first calls at worst repeat the query); 0 on failure.
+int current_attribute(cudaDeviceAttr attr, int* cache) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return 0;
-  if (dev < kMaxDevices && g_sm_count[dev] > 0) return g_sm_count[dev];
-  int sms = 0;
-  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
-  if (dev < kMaxDevices) g_sm_count[dev] = sms;
-  return sms;
+  if (dev < kMaxDevices) {
+    const int v = ep::cache_load(&cache[dev]);
+    if (v > 0) return v;
+  }
+  int v = 0;
+  if (cudaDeviceGetAttribute(&v, attr, dev) != cudaSuccess) return 0;
+  if (dev < kMaxDevices && v > 0) ep::cache_store(&cache[dev], v);
+  return v;
 }
+
+// SM count of the current device; 0 on failure.
+int current_sm_count() { return current_attribute(cudaDevAttrMultiProcessorCount, g_sm_count); }
 
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
@@ -64,16 +71,66 @@ int64_t max_rows_of(const ep_config_t* c) {
 
 ep_status_t from_cuda(cudaError_t e) { return e == cudaSuccess ? EP_OK : EP_ERR_CUDA; }
 
+int g_route_dispatch_form = EP_FORM_AUTO;  // ep_debug_set(EP_DEBUG_ROUTE_DISPATCH_FORM, ...)
+
+// Whether ep_route_dispatch's single cooperative launch beats the kernel
+// chain, by batch shape (measured on the B300): it does for large batches,
+// where every SM takes tokens from one counter and the scan kernel and its
+// boundary go away, and for small ones with E >= 32, where the layout comes
+// from the routed ids; in between (a few thousand tokens) its fixed cost (two
+// device-wide waits, every CTA reading every tile's counts) is more than the
+// chain's, and with E < 32 the cluster form of the chain is quicker.
+bool single_launch_pays(const ep_config_t* c) {
+  if (c->T >= 8192) return true;
+  return static_cast<int64_t>(c->T) * c->k <= 8192 && c->E >= 32;
+}
+
+// The form ep_route_dispatch takes for a call whose arguments passed the
+// checks: the single launch (if chosen and it can run here), the cluster form
+// of the chain for small batches (if such a cluster can be resident), else
+// the three-kernel chain. The checks launch nothing.
+enum class Form { kSingle, kCluster, kChain };
+Form choose_form(const ep_config_t* cfg, const ep::RouteCountArgs& r, const ep::DispatchArgs& a, int sms) {
+  const int form = ep::cache_load(&g_route_dispatch_form);
+  if ((form == EP_FORM_SINGLE || (form == EP_FORM_AUTO && single_launch_pays(cfg))) &&
+      ep::launch_route_dispatch_fused(r, a, sms, nullptr, true) == cudaSuccess)
+    return Form::kSingle;
+  if (ep::small_batch(r.T, r.E, r.tile) && ep::launch_route_layout_small(r, a, nullptr, true) == cudaSuccess)
+    return Form::kCluster;
+  return Form::kChain;
+}
+
+// The routing arguments of ep_route_dispatch (from the checked dispatch ones).
+ep::RouteCountArgs route_count_args(const ep_config_t* cfg, const float* logits, int32_t* topk_idx, float* topk_w,
+                                    const ep::DispatchArgs& a) {
+  ep::RouteCountArgs r;
+  r.logits = logits;
+  r.T = cfg->T;
+  r.E = cfg->E;
+  r.k = cfg->k;
+  r.renorm = cfg->renormalize;
+  r.tile = a.tile;
+  r.ntiles = a.ntiles;
+  r.topk_idx = topk_idx;
+  r.topk_w = topk_w;
+  r.tile_counts = a.tile_counts;
+  r.lrank = a.lrank;
+  r.ticket = a.ticket;
+  return r;
+}
+
 ep_status_t carve_layout(const ep_config_t* cfg, int32_t* expert_counts, int32_t* expert_raw, int32_t* expert_off,
                          int32_t* rank_off, int32_t* n_dropped, void* ws, size_t ws_bytes, ep::DispatchArgs* out,
                          int* sms_out);
 
+}  // namespace
+
 // Checks the dispatch arguments (before any launch) and fills the kernel
 // arguments, with the workspace carved into its regions.
-ep_status_t prepare_dispatch(const ep_config_t* cfg, const void* x, const int32_t* topk_idx, void* payload,
-                             float* scales, int32_t* row_slot, int32_t* slot_row, int32_t* expert_counts,
-                             int32_t* expert_raw, int32_t* expert_off, int32_t* rank_off, int32_t* n_dropped,
-                             void* ws, size_t ws_bytes, ep::DispatchArgs* out, int* sms_out) {
+ep_status_t ep::prepare_dispatch(const ep_config_t* cfg, const void* x, const int32_t* topk_idx, void* payload,
+                                 float* scales, int32_t* row_slot, int32_t* slot_row, int32_t* expert_counts,
+                                 int32_t* expert_raw, int32_t* expert_off, int32_t* rank_off, int32_t* n_dropped,
+                                 void* ws, size_t ws_bytes, ep::DispatchArgs* out, int* sms_out) {
   if (!config_ok(cfg)) return EP_ERR_INVALID_ARG;
   const bool coded = cfg->payload != EP_PAYLOAD_BF16;  // int8 or FP8 code + per-row scale
   if (!expert_counts || !expert_off || !rank_off || !n_dropped) return EP_ERR_INVALID_ARG;
@@ -98,6 +155,8 @@ ep_status_t prepare_dispatch(const ep_config_t* cfg, const void* x, const int32_
   a.slot_row = slot_row;
   return EP_OK;
 }
+
+namespace {
 
 // The layout part of the kernel arguments (sizes, cap, the layout outputs and
 // the workspace regions), after the workspace check.
@@ -131,6 +190,9 @@ ep_status_t carve_layout(const ep_config_t* cfg, int32_t* expert_counts, int32_t
   a.n_dropped = n_dropped;
   a.status = reinterpret_cast<uint32_t*>(w + L.status_off);
   a.ticket = reinterpret_cast<uint32_t*>(w + L.ticket_off);
+  a.bar_count = reinterpret_cast<unsigned*>(w + L.bar_off);
+  a.bar_round = reinterpret_cast<unsigned*>(w + L.bar_off + 128);
+  a.work = reinterpret_cast<unsigned*>(w + L.bar_off + 256);
   a.kept = reinterpret_cast<int32_t*>(w + L.kept_off);
   a.dropped = reinterpret_cast<int32_t*>(w + L.drop_off);
   a.tile_counts = reinterpret_cast<int32_t*>(w + L.tile_counts_off);
@@ -208,7 +270,7 @@ ep_status_t ep_dispatch(const ep_config_t* cfg, const void* x, const int32_t* to
                         void* ws, size_t ws_bytes, cudaStream_t stream) {
   ep::DispatchArgs a;
   int sms = 0;
-  const ep_status_t st = prepare_dispatch(cfg, x, topk_idx, payload, scales, row_slot, slot_row, expert_counts,
+  const ep_status_t st = ep::prepare_dispatch(cfg, x, topk_idx, payload, scales, row_slot, slot_row, expert_counts,
                                           expert_raw, expert_off, rank_off, n_dropped, ws, ws_bytes, &a, &sms);
   if (st != EP_OK) return st;
   return from_cuda(ep::launch_dispatch(a, sms, stream));
@@ -225,30 +287,21 @@ ep_status_t ep_route_dispatch(const ep_config_t* cfg, const float* logits, const
   }
   ep::DispatchArgs a;
   int sms = 0;
-  const ep_status_t st = prepare_dispatch(cfg, x, topk_idx, payload, scales, row_slot, slot_row, expert_counts,
+  const ep_status_t st = ep::prepare_dispatch(cfg, x, topk_idx, payload, scales, row_slot, slot_row, expert_counts,
                                           expert_raw, expert_off, rank_off, n_dropped, ws, ws_bytes, &a, &sms);
   if (st != EP_OK) return st;
-  ep::RouteCountArgs r;
-  r.logits = logits;
-  r.T = cfg->T;
-  r.E = cfg->E;
-  r.k = cfg->k;
-  r.renorm = cfg->renormalize;
-  r.tile = a.tile;
-  r.ntiles = a.ntiles;
-  r.topk_idx = topk_idx;
-  r.topk_w = topk_w;
-  r.tile_counts = a.tile_counts;
-  r.lrank = a.lrank;
-  r.ticket = a.ticket;
-  if (ep::small_batch(r.T, r.E, r.tile)) {  // one cluster routes and lays out the batch, then the scatter
-    const cudaError_t e = ep::launch_route_layout_small(r, a, stream);
-    if (e == cudaSuccess) {
+  ep::RouteCountArgs r = route_count_args(cfg, logits, topk_idx, topk_w, a);
+  switch (choose_form(cfg, r, a, sms)) {
+    case Form::kSingle:  // one cooperative launch routes, lays out and scatters the batch
+      return from_cuda(ep::launch_route_dispatch_fused(r, a, sms, stream));
+    case Form::kCluster: {  // one cluster routes and lays out the batch, then the scatter
+      const cudaError_t e = ep::launch_route_layout_small(r, a, stream);
+      if (e != cudaSuccess) return EP_ERR_CUDA;
       a.pairs_early = 0;  // the routing kernel just before wrote topk_idx and lrank
       return from_cuda(ep::launch_scatter(a, sms, stream));
     }
-    if (e != cudaErrorNotSupported) return EP_ERR_CUDA;
-    // the cluster cannot be resident on this device: the general path below
+    case Form::kChain:
+      break;
   }
   const cudaError_t err = ep::launch_route_count(r, stream);
   if (err != cudaSuccess) return EP_ERR_CUDA;
@@ -334,9 +387,46 @@ ep_status_t ep_get_error(void* ws, size_t ws_bytes, cudaStream_t stream) {
   if (cudaMemcpyAsync(&flags, ws, sizeof flags, cudaMemcpyDeviceToHost, stream) != cudaSuccess) return EP_ERR_CUDA;
   if (cudaStreamSynchronize(stream) != cudaSuccess) return EP_ERR_CUDA;
   if (flags == 0) return EP_OK;
-  if (cudaMemsetAsync(ws, 0, sizeof flags, stream) != cudaSuccess) return EP_ERR_CUDA;
+  // clear the status word; after a timed-out wait also the grid barrier's
+  // words, which a wait that gave up leaves behind
+  const size_t header = ws_bytes < 512 ? ws_bytes : 512;  // status, ticket, barrier words, counter
+  const size_t clear = (flags & ep::kStatusTimeout) ? header : sizeof flags;
+  if (cudaMemsetAsync(ws, 0, clear, stream) != cudaSuccess) return EP_ERR_CUDA;
+  if (cudaStreamSynchronize(stream) != cudaSuccess) return EP_ERR_CUDA;
   if (flags & ep::kStatusTimeout) return EP_ERR_TIMEOUT;
   return EP_ERR_DEVICE_INDEX;
+}
+
+ep_status_t ep_route_dispatch_kernels(const ep_config_t* cfg, int32_t* kernels) {
+  if (!config_ok(cfg) || kernels == nullptr) return EP_ERR_INVALID_ARG;
+  const ep::WsLayout L = ep::ws_layout(cfg->T, cfg->E, cfg->k);
+  ep::DispatchArgs a;
+  int sms = 0;
+  // no buffers: carve a workspace-sized range at address 0 (nothing is read
+  // or launched; x is taken as 32-byte aligned)
+  const ep_status_t st = carve_layout(cfg, nullptr, nullptr, nullptr, nullptr, nullptr,
+                                      reinterpret_cast<void*>(static_cast<uintptr_t>(256)), L.total, &a, &sms);
+  if (st != EP_OK) return st;
+  const ep::RouteCountArgs r = route_count_args(cfg, nullptr, nullptr, nullptr, a);
+  switch (choose_form(cfg, r, a, sms)) {
+    case Form::kSingle: *kernels = 1; break;
+    case Form::kCluster: *kernels = 2; break;
+    case Form::kChain: *kernels = cfg->T > 0 ? 3 : 2; break;  // route+count, scan, scatter (none when empty)
+  }
+  return EP_OK;
+}
+
+ep_status_t ep_debug_set(int32_t option, int32_t value) {
+  switch (option) {
+    case EP_DEBUG_FORCE_WAIT_TIMEOUT:
+      ep::set_force_wait_timeout(value);
+      return EP_OK;
+    case EP_DEBUG_ROUTE_DISPATCH_FORM:
+      if (value < EP_FORM_AUTO || value > EP_FORM_CHAIN) return EP_ERR_INVALID_ARG;
+      ep::cache_store(&g_route_dispatch_form, value);
+      return EP_OK;
+  }
+  return EP_ERR_INVALID_ARG;
 }
 
 ep_status_t ep_load_stats(const int32_t* host_counts, int32_t E, ep_load_stats_t* out) {

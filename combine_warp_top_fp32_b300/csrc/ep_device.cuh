@@ -55,6 +55,40 @@ __device__ __forceinline__ void st_v2(void* p, uint2 v) {
   asm volatile("st.global.v2.u32 [%0], {%1,%2};" ::"l"(p), "r"(v.x), "r"(v.y) : "memory");
 }
 
+// ---- L2 residency ------------------------------------------------------------
+// The dispatch reads x once and writes the payload once; neither is reused
+// within the step. The scatter marks what it touches as the first to be
+// evicted from L2: its x reads (.L2::evict_first) and its payload stores (an
+// evict-first cache policy), so that the payload stream recycles its own
+// lines rather than pushing out lines that are read again (the routing
+// metadata, and the combine's inputs in a step that follows).
+
+// A cache policy under which the lines an access allocates are the first
+// candidates for eviction from L2.
+__device__ __forceinline__ uint64_t l2_evict_first_policy() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+
+__device__ __forceinline__ void st_v4_hint(void* p, uint4 v, uint64_t pol) {
+  asm volatile("st.global.L2::cache_hint.v4.u32 [%0], {%1,%2,%3,%4}, %5;" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z),
+               "r"(v.w), "l"(pol)
+               : "memory");
+}
+
+__device__ __forceinline__ void st_v2_hint(void* p, uint2 v, uint64_t pol) {
+  asm volatile("st.global.L2::cache_hint.v2.u32 [%0], {%1,%2}, %3;" ::"l"(p), "r"(v.x), "r"(v.y), "l"(pol) : "memory");
+}
+
+__device__ __forceinline__ uint4 ld_stream_v4_hint(const void* p, uint64_t pol) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.v4.u32 {%0,%1,%2,%3}, [%4], %5;"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p), "l"(pol));
+  return v;
+}
+
 // ---- bf16 pairs ----------------------------------------------------------
 // A 32-bit word holds two bf16: the low half is the lower-addressed element.
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }

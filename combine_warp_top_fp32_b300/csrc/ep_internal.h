@@ -7,6 +7,7 @@
 
 #include <utility>
 
+#include "ep.h"
 #include "ep_device.cuh"
 
 namespace ep {
@@ -22,13 +23,19 @@ inline int tile_tokens_for(int T, int E) {
   return tile;
 }
 
+// The fused route+layout+scatter kernel (fused.cu): at most this many CTAs
+// (one per SM) and experts (at most 8 logits per routing lane).
+constexpr int kFusedMaxCTAs = 256;
+constexpr int kFusedMaxExperts = 256;
+
 // Workspace layout (each region 256-byte aligned):
-//   [status word, scan ticket | kept E | dropped E | tile_counts E x ntiles |
-//    tile_base E x ntiles | lrank T*k]
+//   [status word, scan ticket | barrier arrivals | barrier round | token counter | kept E |
+//    dropped E | tile_counts E x max(ntiles, fused CTAs) | tile_base E x ntiles |
+//    lrank T*k]
 struct WsLayout {
   int tile;
   int ntiles;
-  size_t status_off, ticket_off, kept_off, drop_off, tile_counts_off, tile_base_off, lrank_off, total;
+  size_t status_off, ticket_off, bar_off, kept_off, drop_off, tile_counts_off, tile_base_off, lrank_off, total;
 };
 
 inline size_t align256(size_t v) { return (v + 255) & ~static_cast<size_t>(255); }
@@ -38,12 +45,18 @@ inline WsLayout ws_layout(int T, int E, int k) {
   L.tile = tile_tokens_for(T, E);
   L.ntiles = (T + L.tile - 1) / L.tile;
   const size_t counters = static_cast<size_t>(E) * static_cast<size_t>(L.ntiles) * sizeof(int32_t);
+  const int fused_ctas = T < kFusedMaxCTAs ? T : kFusedMaxCTAs;
+  const size_t count_slots = static_cast<size_t>(E) *
+                             static_cast<size_t>(L.ntiles > fused_ctas ? L.ntiles : fused_ctas) * sizeof(int32_t);
   L.status_off = 0;
   L.ticket_off = 4;
-  L.kept_off = 256;
+  L.bar_off = 128;  // the grid barrier's arrivals at 128, its round at 256 and the fused scatter's token
+                    // counter at 384, each on a 128-byte line of its own (the round is polled while the
+                    // arrivals are counted, the counter taken from all the while)
+  L.kept_off = 512;
   L.drop_off = L.kept_off + align256(static_cast<size_t>(E) * sizeof(int32_t));
   L.tile_counts_off = L.drop_off + align256(static_cast<size_t>(E) * sizeof(int32_t));
-  L.tile_base_off = L.tile_counts_off + align256(counters);
+  L.tile_base_off = L.tile_counts_off + align256(count_slots);
   L.lrank_off = L.tile_base_off + align256(counters);
   L.total = L.lrank_off + align256(static_cast<size_t>(T) * static_cast<size_t>(k) * sizeof(int32_t));
   return L;
@@ -109,7 +122,7 @@ constexpr int kMaxCluster = 8;  // the portable cluster size
 using ClusterFits = signed char[64][kMaxCluster + 1];
 template <typename... KArgs, typename... Args>
 inline cudaError_t launch_cluster_pdl(void (*kernel)(KArgs...), int grid, int block, size_t smem, cudaStream_t s,
-                                      ClusterFits& fits, Args&&... args) {
+                                      ClusterFits& fits, bool dry, Args&&... args) {
   if (grid < 1 || grid > kMaxCluster) return cudaErrorNotSupported;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(grid));
@@ -140,6 +153,7 @@ inline cudaError_t launch_cluster_pdl(void (*kernel)(KArgs...), int grid, int bl
     if (dev < 64) cache_store(&fits[dev][grid], f);
   }
   if (f < 0) return cudaErrorNotSupported;
+  if (dry) return cudaSuccess;
   cfg.numAttrs = 2;
   return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
@@ -158,6 +172,8 @@ struct DispatchArgs {
   // workspace regions
   uint32_t* status;
   uint32_t* ticket;
+  unsigned *bar_count, *bar_round;  // the fused kernel's grid barrier
+  unsigned* work;                   // the fused kernel's scatter token counter
   int32_t *kept, *dropped, *tile_counts, *tile_base, *lrank;
   int tile, ntiles;
   // 1 when the pair data (topk_idx, lrank) was written two or more launches
@@ -165,6 +181,14 @@ struct DispatchArgs {
   // 0 when the kernel just before the scatter wrote it.
   int pairs_early = 1;
 };
+
+// Checks the arguments of a dispatch (before any launch: a status other than
+// EP_OK means nothing was enqueued) and fills the kernel arguments, with the
+// workspace ws carved into its regions; *sms_out is the device's SM count.
+ep_status_t prepare_dispatch(const ep_config_t* cfg, const void* x, const int32_t* topk_idx, void* payload,
+                             float* scales, int32_t* row_slot, int32_t* slot_row, int32_t* expert_counts,
+                             int32_t* expert_raw, int32_t* expert_off, int32_t* rank_off, int32_t* n_dropped,
+                             void* ws, size_t ws_bytes, DispatchArgs* out, int* sms_out);
 
 // ep_dispatch: count kernel, then scan and scatter.
 cudaError_t launch_dispatch(const DispatchArgs& a, int sms, cudaStream_t s);
@@ -201,7 +225,22 @@ cudaError_t launch_route_count(const RouteCountArgs& r, cudaStream_t s);
 constexpr int kClusterTiles = kMaxCluster;
 constexpr int kClusterExperts = 256;  // experts per routing lane group of 32: at most 8 values per lane
 bool small_batch(int T, int E, int tile);
-cudaError_t launch_route_layout_small(const RouteCountArgs& r, const DispatchArgs& a, cudaStream_t s);
+cudaError_t launch_route_layout_small(const RouteCountArgs& r, const DispatchArgs& a, cudaStream_t s,
+                                      bool dry = false);
+
+// ep_route_dispatch in one cooperative launch of one CTA per SM (fused.cu):
+// routing, layout and scatter with one bounded grid barrier. Returns
+// cudaErrorNotSupported, having launched nothing, when the problem or the
+// device does not suit it (E > kFusedMaxExperts, more than 1024 tokens per
+// SM, x not 32-byte aligned, no cooperative launch); the caller then takes
+// the kernel chain.
+// dry: check only (the same checks, nothing launched): cudaSuccess when it would run.
+cudaError_t launch_route_dispatch_fused(const RouteCountArgs& r, const DispatchArgs& a, int sms, cudaStream_t s,
+                                        bool dry = false);
+// Test hook (ep_debug_force_wait_timeout): the fused kernel's grid barrier
+// waits for one CTA more than the grid, with a short limit, so that it runs
+// out and reports EP_ERR_TIMEOUT.
+void set_force_wait_timeout(int enable);
 
 struct CombineArgs {
   int T, H, k;

@@ -30,14 +30,14 @@ static __device__ __align__(256) unsigned char g_dispatch_scratch[EP_STATIC_SCRA
 namespace {
 
 constexpr int kMaxDevices = 64;
-void* g_scratch_ptr[kMaxDevices];  // device address of g_dispatch_scratch, per device
-int g_scratch_sms[kMaxDevices];
+// Device address of g_dispatch_scratch, per device: one pointer, read and
+// written with relaxed atomics, so concurrent first calls on a device at
+// worst both look the address up (and store the same value).
+void* g_scratch_ptr[kMaxDevices];
 
-bool is_aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
-
-// Device address of the static scratch on the current device (set up on the
-// first call per device). Returns nullptr and sets *err on failure.
-void* static_scratch(int* sms, cudaError_t* err) {
+// Device address of the static scratch on the current device (looked up on
+// the first call per device). Returns nullptr and sets *err on failure.
+void* static_scratch(cudaError_t* err) {
   int dev = 0;
   *err = cudaGetDevice(&dev);
   if (*err != cudaSuccess) return nullptr;
@@ -45,18 +45,13 @@ void* static_scratch(int* sms, cudaError_t* err) {
     *err = cudaErrorInvalidDevice;
     return nullptr;
   }
-  if (g_scratch_ptr[dev] == nullptr) {
-    void* p = nullptr;
+  void* p = ep::cache_load(&g_scratch_ptr[dev]);
+  if (p == nullptr) {
     *err = cudaGetSymbolAddress(&p, g_dispatch_scratch);
     if (*err != cudaSuccess) return nullptr;
-    int n = 0;
-    *err = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-    if (*err != cudaSuccess) return nullptr;
-    g_scratch_sms[dev] = n;
-    g_scratch_ptr[dev] = p;
+    ep::cache_store(&g_scratch_ptr[dev], p);
   }
-  *sms = g_scratch_sms[dev];
-  return g_scratch_ptr[dev];
+  return p;
 }
 
 }  // namespace
@@ -65,60 +60,25 @@ extern "C" ep_status_t ep_dispatch_static(const ep_config_t* cfg, const void* x,
                                           void* payload, float* scales, int32_t* row_slot, int32_t* slot_row,
                                           int32_t* expert_counts, int32_t* expert_raw, int32_t* expert_off,
                                           int32_t* rank_off, int32_t* n_dropped, cudaStream_t stream) {
+  // The size check comes first and needs no device: a problem whose scratch
+  // does not fit the fixed array is refused before anything is enqueued.
   if (ep_config_check(cfg) != EP_OK) return EP_ERR_INVALID_ARG;
-  const bool coded = cfg->payload != EP_PAYLOAD_BF16;  // int8 or FP8 code + per-row scale
-  if (!expert_counts || !expert_off || !rank_off || !n_dropped) return EP_ERR_INVALID_ARG;
-  if (cfg->T > 0) {
-    if (!x || !topk_idx || !payload || !row_slot || !slot_row) return EP_ERR_INVALID_ARG;
-    if (coded && !scales) return EP_ERR_INVALID_ARG;
-    if (!is_aligned(x, 16) || !is_aligned(payload, 16)) return EP_ERR_INVALID_ARG;
-  }
-  if (!is_aligned(topk_idx, 4) || !is_aligned(row_slot, 4) || !is_aligned(slot_row, 4) ||
-      !is_aligned(expert_counts, 4) || !is_aligned(expert_raw, 4) || !is_aligned(expert_off, 4) ||
-      !is_aligned(rank_off, 4) || !is_aligned(n_dropped, 4) || !is_aligned(scales, 4))
-    return EP_ERR_INVALID_ARG;
-  // The problem's scratch must fit the fixed array; larger problems are
-  // refused here, before anything is enqueued.
   const ep::WsLayout L = ep::ws_layout(cfg->T, cfg->E, cfg->k);
   if (L.total > static_cast<size_t>(EP_STATIC_SCRATCH_BYTES)) return EP_ERR_WORKSPACE;
 
-  int sms = 0;
   cudaError_t err = cudaSuccess;
-  char* w = static_cast<char*>(static_scratch(&sms, &err));
-  if (w == nullptr || sms <= 0) return EP_ERR_CUDA;
+  void* w = static_scratch(&err);
+  if (w == nullptr) return EP_ERR_CUDA;
+  // The same argument checks and workspace carving as ep_dispatch, over the
+  // static array (nothing is enqueued unless they pass).
+  ep::DispatchArgs a;
+  int sms = 0;
+  const ep_status_t st = ep::prepare_dispatch(cfg, x, topk_idx, payload, scales, row_slot, slot_row, expert_counts,
+                                              expert_raw, expert_off, rank_off, n_dropped, w,
+                                              static_cast<size_t>(EP_STATIC_SCRATCH_BYTES), &a, &sms);
+  if (st != EP_OK) return st;
   // The array keeps the previous call's contents: clear the status word and
   // the scan ticket, the only parts read before this call writes them.
   if (cudaMemsetAsync(w, 0, 256, stream) != cudaSuccess) return EP_ERR_CUDA;
-
-  ep::DispatchArgs a;
-  a.T = cfg->T;
-  a.H = cfg->H;
-  a.E = cfg->E;
-  a.k = cfg->k;
-  a.R = cfg->R;
-  int32_t cap = 0;
-  if (ep_capacity(cfg, &cap) != EP_OK) return EP_ERR_INVALID_ARG;
-  a.cap = cap;
-  a.fmt = cfg->payload;
-  a.x = x;
-  a.topk_idx = topk_idx;
-  a.payload = payload;
-  a.scales = scales;
-  a.row_slot = row_slot;
-  a.slot_row = slot_row;
-  a.expert_counts = expert_counts;
-  a.expert_raw = expert_raw;
-  a.expert_off = expert_off;
-  a.rank_off = rank_off;
-  a.n_dropped = n_dropped;
-  a.status = reinterpret_cast<uint32_t*>(w + L.status_off);
-  a.ticket = reinterpret_cast<uint32_t*>(w + L.ticket_off);
-  a.kept = reinterpret_cast<int32_t*>(w + L.kept_off);
-  a.dropped = reinterpret_cast<int32_t*>(w + L.drop_off);
-  a.tile_counts = reinterpret_cast<int32_t*>(w + L.tile_counts_off);
-  a.tile_base = reinterpret_cast<int32_t*>(w + L.tile_base_off);
-  a.lrank = reinterpret_cast<int32_t*>(w + L.lrank_off);
-  a.tile = L.tile;
-  a.ntiles = L.ntiles;
   return ep::launch_dispatch(a, sms, stream) == cudaSuccess ? EP_OK : EP_ERR_CUDA;
 }

@@ -173,23 +173,43 @@ ep_status_t ep_dispatch(const ep_config_t* cfg, const void* x, const int32_t* to
 
 /*
  * ep_route_dispatch — ep_route followed by ep_dispatch in one call, with the
- * routing fused into the dispatch's per-tile count (ThunderEP on consumer
- * GPUs, bjdmk.com.cn, §5.2: do the bucketing by destination while routing,
- * saving a pass). Every output is bit-for-bit what
+ * routing fused into the dispatch (ThunderEP on consumer GPUs, bjdmk.com.cn,
+ * §5.2: do the bucketing by destination while routing, saving a pass; the
+ * Perseus summary, itsolotime.com, §1.3: one persistent kernel for the whole
+ * exchange). Every output is bit-for-bit what
  *   ep_route(cfg, logits, topk_idx, topk_w, stream);
  *   ep_dispatch(cfg, x, topk_idx, payload, ..., ws, ws_bytes, stream);
  * would write; the arguments mean what they mean there (logits [T, E] fp32
- * in, 16-byte aligned; topk_idx / topk_w [T, k] out). One kernel fewer runs:
- * a CTA routes one tile of tokens and counts its per-expert copies in shared
- * memory, then the scan and the scatter run as in ep_dispatch. A batch of at
- * most 256 tokens with E <= 256 takes two kernels: one thread-block cluster
- * routes it and forms the whole layout, then the scatter (where such a
- * cluster cannot be resident, the three-kernel form runs instead).
+ * in, 16-byte aligned; topk_idx / topk_w [T, k] out).
+ * Single-launch form (large batches, T >= 8192, and small ones, T*k <= 8192
+ * with 32 <= E; E <= 256, at most 1024 tokens per SM, x 32-byte aligned,
+ * cooperative launch available): one cooperative launch of one CTA per SM
+ * does it all. Each CTA routes its own tile of ceil(T / SMs) tokens; one
+ * device-wide wait; each CTA forms its tile's positions from every tile's
+ * counts (small batches: from all the routed ids) and writes its pairs' rows;
+ * then the payload is scattered, each SM taking tokens from a shared counter
+ * (a second device-wide wait first), or, for small batches, each CTA its own
+ * tile. Those waits are bounded (about a second); if one runs out the call's
+ * outputs are not valid and ep_get_error() reports EP_ERR_TIMEOUT (and resets
+ * the waits' words in the workspace, so the workspace can be used again).
+ * Otherwise three kernels run: a CTA routes one tile of tokens and counts its
+ * per-expert copies in shared memory, then the scan and the scatter of
+ * ep_dispatch; a batch of at most 256 tokens with E <= 256 then takes two
+ * (one thread-block cluster routes it and forms the whole layout, then the
+ * scatter).
  */
 ep_status_t ep_route_dispatch(const ep_config_t* cfg, const float* logits, const void* x, int32_t* topk_idx,
                               float* topk_w, void* payload, float* scales, int32_t* row_slot, int32_t* slot_row,
                               int32_t* expert_counts, int32_t* expert_raw, int32_t* expert_off, int32_t* rank_off,
                               int32_t* n_dropped, void* ws, size_t ws_bytes, cudaStream_t stream);
+
+/*
+ * ep_route_dispatch_kernels — how many kernels ep_route_dispatch launches for
+ * `cfg` on the current device (1: the single cooperative launch; 2: the
+ * cluster form; 3: the chain, or 2 for an empty batch), taking x as 32-byte
+ * aligned; host only, launches nothing. *kernels out.
+ */
+ep_status_t ep_route_dispatch_kernels(const ep_config_t* cfg, int32_t* kernels);
 
 /*
  * ep_bitmap_encode — compact routing metadata (MoE sparse-communication
@@ -314,9 +334,28 @@ ep_status_t ep_quantize_rows_int4(const void* in, int64_t n, int32_t H, uint8_t*
 /*
  * ep_get_error — synchronises `stream`, reads the workspace's status word,
  * clears it, and returns EP_OK, EP_ERR_DEVICE_INDEX or EP_ERR_TIMEOUT (or
- * EP_ERR_CUDA if the stream itself failed). The one call that blocks.
+ * EP_ERR_CUDA if the stream itself failed). The one call that blocks. After
+ * EP_ERR_TIMEOUT it also resets the words of the device-wide waits.
  */
 ep_status_t ep_get_error(void* ws, size_t ws_bytes, cudaStream_t stream);
+
+/*
+ * ep_debug_set — process-wide test hooks (not for production use); returns
+ * EP_OK, or EP_ERR_INVALID_ARG for an unknown option.
+ *   EP_DEBUG_FORCE_WAIT_TIMEOUT (value 0/1): while set, the device-wide wait
+ *     of ep_route_dispatch's single-launch form counts one CTA more than the
+ *     launch has and gives up after about a millisecond, so every such call
+ *     made meanwhile reports EP_ERR_TIMEOUT through ep_get_error() and leaves
+ *     its outputs invalid (the NCCL EP article, §4.2-4.3: a wait that cannot
+ *     complete must end in an error, not a hang).
+ *   EP_DEBUG_ROUTE_DISPATCH_FORM (value EP_FORM_*): which form of
+ *     ep_route_dispatch runs: the library's choice by batch shape (AUTO), the
+ *     single cooperative launch wherever it can run (SINGLE), or the kernel
+ *     chain (CHAIN). Every form writes the same bytes.
+ */
+typedef enum { EP_DEBUG_FORCE_WAIT_TIMEOUT = 1, EP_DEBUG_ROUTE_DISPATCH_FORM = 2 } ep_debug_option_t;
+typedef enum { EP_FORM_AUTO = 0, EP_FORM_SINGLE = 1, EP_FORM_CHAIN = 2 } ep_route_dispatch_form_t;
+ep_status_t ep_debug_set(int32_t option, int32_t value);
 
 /*
  * Load statistics over per-expert counts already copied to the host

@@ -128,3 +128,19 @@ def test_int4_payload_needs_h_multiple_of_32(ep):
     assert ep.ep_config_check(ok) == ep.EP_OK
     assert ep.ep_config_check(bad) == ep.EP_ERR_INVALID_ARG
     assert ep.ep_config_check(ep.make_config(64, 48, 8, 2, 2, payload=4)) == ep.EP_ERR_INVALID_ARG
+
+
+def test_debug_hooks_reject_unknown_options(ep):
+    # only invalid values: a valid one would change process-wide state
+    assert ep.lib.ep_debug_set(99, 0) == ep.EP_ERR_INVALID_ARG
+    assert ep.lib.ep_debug_set(ep.EP_DEBUG_ROUTE_DISPATCH_FORM, 7) == ep.EP_ERR_INVALID_ARG
+    assert ep.lib.ep_debug_set(ep.EP_DEBUG_ROUTE_DISPATCH_FORM, -1) == ep.EP_ERR_INVALID_ARG
+
+
+def test_route_dispatch_kernels_checks_its_arguments(ep):
+    bad = ep.make_config(16, 15, 8, 2, 2)  # H not a multiple of 16
+    n = ctypes.c_int32(-1)
+    assert ep.lib.ep_route_dispatch_kernels(ctypes.byref(bad), ctypes.byref(n)) == ep.EP_ERR_INVALID_ARG
+    good = ep.make_config(16, 64, 8, 2, 2)
+    assert ep.lib.ep_route_dispatch_kernels(ctypes.byref(good), None) == ep.EP_ERR_INVALID_ARG
+    assert n.value == -1

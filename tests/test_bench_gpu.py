@@ -32,8 +32,13 @@ def test_bench_line_on_decode_latency(monkeypatch):
     assert d["unit"] == "tokens/s" and d["higher_is_better"] is True and d["n_gpus"] == 1
     assert d["value"] > 0
     assert d["value"] == pytest.approx(w.T / (d["ms_per_step"] / 1e3), rel=1e-6)
-    # the batch is laid out by one cluster launch: route+layout, scatter, combine
-    assert d["gpu_launches"] == 3 * steps
+    # ep_route_dispatch as the library reports it (on this part, the decode
+    # batch takes the single cooperative launch), then the combine
+    from combine_warp_top_fp32_b300 import binding as ep
+
+    kernels = ep.ep_route_dispatch_kernels(ep.config_from_workload(w, payload=ep.EP_PAYLOAD_INT8))
+    assert kernels == 1
+    assert d["gpu_launches"] == (kernels + 1) * steps
     assert d["config"]["workload"] == "decode-latency" and d["config"]["payload"] == "int8"
 
     roof = d["roofline"]

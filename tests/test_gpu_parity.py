@@ -42,18 +42,26 @@ _OUTPUTS = ("topk_idx", "topk_w", "slot_row", "expert_counts", "expert_raw", "ex
 
 
 def _assert_fused_matches(ep, cfg, ref, logits, x):
-    """ep_route_dispatch writes bit-for-bit what ep_route + ep_dispatch wrote."""
-    fused = ep.EpBuffers.allocate(cfg)
-    fused.route_dispatch(logits, x)
-    torch.cuda.synchronize()
-    assert ep.ep_get_error(fused.ws) == ep.EP_OK
-    for name in _OUTPUTS:
-        assert torch.equal(getattr(ref, name), getattr(fused, name)), name
-    N = int(ref.rank_off[-1].item())
-    assert torch.equal(ref.row_slot[:N], fused.row_slot[:N])
-    assert torch.equal(ref.payload[:N].view(torch.uint8), fused.payload[:N].view(torch.uint8))
-    if ref.scales is not None:
-        assert torch.equal(ref.scales[:N], fused.scales[:N])
+    """ep_route_dispatch writes bit-for-bit what ep_route + ep_dispatch wrote,
+    in each of its forms: the library's choice, the single cooperative launch
+    (where the shape allows it) and the kernel chain."""
+    try:
+        for form in (ep.EP_FORM_AUTO, ep.EP_FORM_SINGLE, ep.EP_FORM_CHAIN):
+            ep.ep_debug_set(ep.EP_DEBUG_ROUTE_DISPATCH_FORM, form)
+            fused = ep.EpBuffers.allocate(cfg)
+            fused.route_dispatch(logits, x)
+            torch.cuda.synchronize()
+            assert ep.ep_get_error(fused.ws) == ep.EP_OK
+            for name in _OUTPUTS:
+                assert torch.equal(getattr(ref, name), getattr(fused, name)), (form, name)
+            N = int(ref.rank_off[-1].item())
+            assert torch.equal(ref.row_slot[:N], fused.row_slot[:N]), form
+            assert torch.equal(ref.payload[:N].view(torch.uint8), fused.payload[:N].view(torch.uint8)), form
+            if ref.scales is not None:
+                assert torch.equal(ref.scales[:N], fused.scales[:N]), form
+            del fused
+    finally:
+        ep.ep_debug_set(ep.EP_DEBUG_ROUTE_DISPATCH_FORM, ep.EP_FORM_AUTO)
 
 
 def _check_layout(buf, lay, N):
@@ -439,3 +447,42 @@ def test_bad_slot_rows_are_reported(ep):
     yf = y.float().cpu().numpy()
     assert np.all(yf[2] == 0.5) and np.all(yf[3] == 0.5)  # slots 5 and 6 skipped
     assert np.all(yf[0] == 1.0)
+
+
+# ----------------------------------------------------------------------------
+# the fused dispatch's device-wide wait: bounded, reported, recoverable
+# ----------------------------------------------------------------------------
+def test_fused_wait_timeout_is_reported_and_recovers(ep):
+    """With the test hook on, the one grid barrier of the fused route+dispatch
+    kernel waits for a CTA that does not exist and gives up after a short
+    limit: the call reports EP_ERR_TIMEOUT through ep_get_error (no hang, no
+    fault), and the same workspace then serves a normal call whose outputs
+    match the three-call path."""
+    from combine_warp_top_fp32_b300 import workloads
+
+    w = workloads.WORKLOADS["prefill-mid"]
+    cfg = ep.config_from_workload(w, payload=ep.EP_PAYLOAD_INT8)
+    d = workloads.generate(w, device="cuda", expert_out=False)
+    buf = ep.EpBuffers.allocate(cfg)
+    ep.ep_debug_set(ep.EP_DEBUG_ROUTE_DISPATCH_FORM, ep.EP_FORM_SINGLE)
+    ep.ep_debug_set(ep.EP_DEBUG_FORCE_WAIT_TIMEOUT, 1)
+    try:
+        buf.route_dispatch(d["logits"], d["x"])
+        assert ep.ep_get_error(buf.ws) == ep.EP_ERR_TIMEOUT
+    finally:
+        ep.ep_debug_set(ep.EP_DEBUG_FORCE_WAIT_TIMEOUT, 0)
+    ref = ep.EpBuffers.allocate(cfg)
+    ref.route(d["logits"])
+    ref.dispatch(d["x"])
+    torch.cuda.synchronize()
+    assert ep.ep_get_error(ref.ws) == ep.EP_OK
+    _assert_fused_matches(ep, cfg, ref, d["logits"], d["x"])
+    try:
+        buf.route_dispatch(d["logits"], d["x"])  # the workspace that timed out, reused
+        torch.cuda.synchronize()
+        assert ep.ep_get_error(buf.ws) == ep.EP_OK
+    finally:
+        ep.ep_debug_set(ep.EP_DEBUG_ROUTE_DISPATCH_FORM, ep.EP_FORM_AUTO)
+    N = int(ref.rank_off[-1].item())
+    assert torch.equal(ref.slot_row, buf.slot_row)
+    assert torch.equal(ref.payload[:N], buf.payload[:N])
