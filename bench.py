@@ -198,6 +198,8 @@ def oracle_sample_tokens(w, target_s=2.0, probe_tokens=256):
 
 
 _oracle_cache = {}
+_last_oracle_rows = [None]  # rows dispatched by the last oracle pass
+_oracle_generator = [None]  # where the cached oracle inputs were drawn ("cuda": the GPU arm's bytes)
 
 
 def _oracle_inputs(w, n_tokens):
@@ -208,9 +210,13 @@ def _oracle_inputs(w, n_tokens):
     key = (w.name, n_tokens)
     if key not in _oracle_cache:
         ws = w.replace(T=n_tokens)
-        d = workloads.generate(ws, device="cpu")
+        # the whole workload on a GPU machine: the device generator, as the GPU arm
+        # draws it, copied to the host (the same bytes); else the host generator
+        dev = "cuda" if n_tokens == w.T and torch.cuda.is_available() else "cpu"
+        d = {k: v.cpu() for k, v in workloads.generate(ws, device=dev).items()}
         _oracle_cache.clear()
         _oracle_cache[key] = (ws, d["logits"].numpy(), workloads.bf16_bits(d["x"]), workloads.bf16_bits(d["expert_out"]))
+        _oracle_generator[0] = dev
     return _oracle_cache[key]
 
 
@@ -221,8 +227,10 @@ def oracle_pass_seconds(w, n_tokens, payload_int8=None):
     orc = oracle.Oracle()
     p8 = int(w.payloads[0]) if payload_int8 is None else int(payload_int8)  # oracle payload mode
     t0 = time.perf_counter()
-    orc.forward(logits, x_bits, eo_bits, ws.k, ws.R, ws.capacity_factor, ws.renormalize, p8)
-    return time.perf_counter() - t0
+    out = orc.forward(logits, x_bits, eo_bits, ws.k, ws.R, ws.capacity_factor, ws.renormalize, p8)
+    dt = time.perf_counter() - t0
+    _last_oracle_rows[0] = int(out["N"])
+    return dt
 
 
 def run_reference(args):
@@ -240,12 +248,20 @@ def run_reference(args):
     total = sum(times)
     value = n * args.steps / total
     cores = 1
-    sample = f"first {n} of {w.T} tokens of the '{w.name}' workload per step (an instance of the same shape with T={n})"
+    if n == w.T and _oracle_generator[0] == "cuda":
+        sample = f"the whole '{w.name}' workload ({w.T} tokens) per step, the same bytes the GPU arm times"
+    elif n == w.T:
+        sample = (f"the whole '{w.name}' workload ({w.T} tokens) per step, drawn by the host generator "
+                  f"(no GPU here: not the GPU arm's bytes)")
+    else:
+        sample = (f"first {n} of {w.T} tokens of the '{w.name}' workload per step "
+                  f"(an instance of the same shape with T={n})")
+    rows = _last_oracle_rows[0] if n == w.T else None
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "fp32",
-        "data": "synthetic", "config": dict(workload_config(w, args.payload, None, False, args.path),
+        "data": "synthetic", "config": dict(workload_config(w, args.payload, rows, False, args.path),
                                             path="CPU oracle (route, layout, payload, combine)", launch="host"),
         "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle", "sample": sample,
                          "cpu": cpu_model()},
@@ -282,6 +298,88 @@ def workload_config(w, payload, n_rows, eager=False, path="fused"):
 # ----------------------------------------------------------------------------
 # the GPU arm
 # ----------------------------------------------------------------------------
+def graph_stage_ms(stage_fns, steps):
+    """Total and per-stage ms per step of `steps` steps of the stage callables,
+    replayed as one CUDA graph after an untimed replay; stage times from
+    event-record nodes on a side branch (as in the headline measurement)."""
+    import torch
+
+    names = list(stage_fns)
+    stream = torch.cuda.current_stream()
+    ev_start = torch.cuda.Event(enable_timing=True, external=True)
+    ev = [[torch.cuda.Event(enable_timing=True, external=True) for _ in names] for _ in range(steps)]
+    side = torch.cuda.Stream()
+    warm = torch.cuda.Stream()
+    warm.wait_stream(stream)
+    with torch.cuda.stream(warm):
+        for fn in stage_fns.values():
+            fn()
+    stream.wait_stream(warm)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        main = torch.cuda.current_stream()
+        ev_start.record(main)
+        for i in range(steps):
+            for j, n in enumerate(names):
+                stage_fns[n]()
+                side.wait_stream(main)
+                ev[i][j].record(side)
+        main.wait_stream(side)
+    graph.replay()
+    torch.cuda.synchronize()
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    graph.replay()
+    t1.record(stream)
+    torch.cuda.synchronize()
+    ends = [e for step in ev for e in step]
+    starts = [ev_start] + ends[:-1]
+    stage_ms = {n: 0.0 for n in names}
+    for q, (s0, s1) in enumerate(zip(starts, ends)):
+        stage_ms[names[q % len(names)]] += s0.elapsed_time(s1) / steps
+    del graph
+    return t0.elapsed_time(t1) / steps, stage_ms
+
+
+def large_records(steps, peak, peak_src):
+    """The T=131072, H=8192 workload (the target's second config) timed beside
+    the headline, int8 and bf16 payloads, ep_route_dispatch + ep_combine."""
+    import torch
+
+    from combine_warp_top_fp32_b300 import binding as ep
+    from combine_warp_top_fp32_b300 import workloads
+
+    w = workloads.WORKLOADS["large"]
+    d = workloads.generate(w, device="cuda")
+    out = {}
+    for payload in ("int8", "bf16"):
+        p8 = PAYLOAD_MODE[payload]
+        cfg = ep.config_from_workload(w, payload=p8)
+        buf = ep.EpBuffers.allocate(cfg)
+        fns = {"route+dispatch": lambda: buf.route_dispatch(d["logits"], d["x"]),
+               "combine": lambda: buf.combine(d["expert_out"])}
+        ms, stage_ms = graph_stage_ms(fns, steps)
+        assert ep.ep_get_error(buf.ws) == ep.EP_OK
+        N = int(buf.rank_off[-1].item())
+        nb = algorithmic_bytes(w.T, w.H, w.E, w.k, N, p8 != 0, payload_bytes=PAYLOAD_BYTES[payload])
+        gbs = nb["total"] / (ms / 1e3) / 1e9
+        comb_gbs = nb["combine"] / (stage_ms["combine"] / 1e3) / 1e9
+        out[payload] = {
+            "ms_per_step": ms, "value": w.T / (ms / 1e3), "unit": "tokens/s", "steps": steps,
+            "bytes_per_step": nb["total"], "gbs": gbs, "frac_of_8000": gbs / NOMINAL_HBM_GBS,
+            f"frac_of_{peak_src}": gbs / peak,
+            "stages_ms": stage_ms,
+            "roofline": {"bound": "hbm", "kernel": "combine_kernel<bf16>", "achieved": comb_gbs, "peak": peak,
+                         "unit": "GB/s", "frac": comb_gbs / peak, "algorithmic_bytes_per_launch": nb["combine"]},
+            "gpu_launches": (ep.ep_route_dispatch_kernels(cfg) + 1) * steps,
+        }
+        del buf, fns
+        torch.cuda.empty_cache()
+    del d
+    torch.cuda.empty_cache()
+    return out
+
+
 def run_gpu(args):
     import torch
     import torch.distributed as dist
@@ -519,6 +617,41 @@ def run_gpu(args):
                "d2h_bytes_per_step": buf.y.numel() * 2, "steps": k2,
                "note": "H2D logits + x, D2H y each step, double buffered on three streams; "
                        "expert outputs are the device-resident stand-in"}
+        # the host link's own bound for these copies, measured in this run:
+        # the step's H2D alone, its D2H alone, and both at once on the two
+        # copy streams; the loop cannot beat the slowest of (both copies at
+        # once, the device step), so its fraction of that bound says how much
+        # of the e2e time the schedule itself loses
+        def copy_ms(do_h2d, do_d2h, reps=5):
+            c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            torch.cuda.synchronize()
+            c0.record(s_in)
+            s_out.wait_event(c0)
+            for _ in range(reps):
+                if do_h2d:
+                    with torch.cuda.stream(s_in):
+                        d_in[0][0].copy_(h_logits, non_blocking=True)
+                        d_in[0][1].copy_(h_x, non_blocking=True)
+                if do_d2h:
+                    with torch.cuda.stream(s_out):
+                        h_y[0].copy_(bufs[0].y, non_blocking=True)
+            s_in.wait_stream(s_out)
+            c1.record(s_in)
+            torch.cuda.synchronize()
+            return c0.elapsed_time(c1) / reps
+
+        t_h2d, t_d2h, t_both = copy_ms(True, False), copy_ms(False, True), copy_ms(True, True)
+        bound_ms = max(t_both, ms_per_step)
+        e2e_ms = 1e3 * e2e_s / k2
+        e2e["link"] = {"h2d_gbs": h2d / (t_h2d / 1e3) / 1e9, "d2h_gbs": buf.y.numel() * 2 / (t_d2h / 1e3) / 1e9,
+                       "h2d_ms": t_h2d, "d2h_ms": t_d2h, "both_ms": t_both, "device_step_ms": ms_per_step,
+                       "bound_ms_per_step": bound_ms, "e2e_ms_per_step": e2e_ms, "frac_of_bound": bound_ms / e2e_ms,
+                       "note": "pinned host buffers; both = the step's H2D and D2H at once on two streams"}
+
+    # the target's second configuration beside the headline (one GPU runs)
+    large = None
+    if args.workload == "capacity" and not args.no_large and world == 1:
+        large = large_records(args.large_steps, peak, peak_src)
 
     cpu_baseline = None
     if rank == 0 and not args.no_cpu_baseline:
@@ -547,6 +680,8 @@ def run_gpu(args):
         }
         if both is not None:
             line["int8_both_directions"] = both
+        if large is not None:
+            line["large"] = large
         print(json.dumps(line))
     if world > 1:
         dist.destroy_process_group()
@@ -691,13 +826,17 @@ def parse_args(argv=None):
     ap.add_argument("--bitmap", action="store_true",
                     help="report the bitmap routing metadata (bytes saved, encode and layout times)")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-large", action="store_true",
+                    help="skip the T=131072, H=8192 record that the capacity line carries beside the headline")
+    ap.add_argument("--large-steps", type=int, default=5)
     ap.add_argument("--eager", action="store_true", help="launch through the binding each step (no CUDA graph)")
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-int8-return", action="store_true",
                     help="skip the extra line with int8 expert outputs (int8 payload only)")
     ap.add_argument("--cpu-baseline-s", type=float, default=15.0)
-    ap.add_argument("--reference-step-s", type=float, default=2.0)
+    ap.add_argument("--reference-step-s", type=float, default=4.0,
+                    help="longest oracle pass per reference step; the whole workload when it fits (capacity: ~2 s)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

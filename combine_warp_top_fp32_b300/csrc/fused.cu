@@ -1,33 +1,34 @@
 // fused.cu — ep_route_dispatch in one persistent launch: route, lay out and
-// scatter a batch with one CTA per SM and one device-wide wait.
+// scatter a batch with one CTA per SM.
 //
 // The ThunderEP article (bjdmk.com.cn, §5.2) suggests fusing the bucketing by
 // destination with the routing; the Perseus summary (itsolotime.com, §1.3)
 // runs the whole exchange as one persistent kernel. Here, on one GPU, one
 // cooperative launch of G CTAs (one per SM) does the three steps of the
-// dispatch, each CTA on its own tile of consecutive tokens
-// (tile = ceil(T / G), so every SM routes and moves the same number of
-// tokens):
+// dispatch, each CTA routing its own tile of consecutive tokens
+// (tile = ceil(T / G), so every SM routes the same number of tokens):
 //
 //   A  route the tile (route_device.cuh): topk_idx / topk_w, and per-expert
 //      bit masks of the tile's tokens in shared memory, whose popcounts give
 //      the tile's count per expert (written to counts[b][e]) and every pair's
-//      rank within the tile in token order. Meanwhile the copy engine brings
-//      the x rows of the tile's last tokens into shared memory: HBM is
-//      otherwise idle while routing runs.
-//   -- grid barrier (grid_sync.cuh): every tile's counts are written --
-//   B  every CTA reads all G x E counts and forms, for each expert, the
-//      number of its pairs in earlier tiles (this tile's first position
-//      within the expert) and its total; the capacity clip, the expert and
-//      rank offsets follow (NCCL EP article, hotelren.com, §3.3: running sums
-//      of the send counts). CTA 0 writes the layout outputs. No second
-//      barrier: each CTA needs only its own tile's positions.
-//   C  scatter the tile's tokens: rows from the masks and offsets in shared
-//      memory (slot_row / row_slot), then the payload: bf16 copies (a warp
-//      per token) or the per-token int8 / FP8 / int4 code (ThunderEP §2.3;
-//      a group of warps per token with its own named barrier), x read from
-//      shared memory for the preloaded tokens and from global memory for the
-//      rest, the next token's row loaded while this one is coded.
+//      rank within the tile in token order. Small batches only: meanwhile the
+//      copy engine brings the tile's x rows into shared memory.
+//   -- grid barrier 1 (grid_sync.cuh): every tile's routing is written --
+//   B  every CTA forms, for each expert, the number of its pairs in earlier
+//      tiles (this tile's first position within the expert) and its total:
+//      from all G x E tile counts, or, for small batches, from all T*k routed
+//      ids. The capacity clip and the expert and rank offsets follow (NCCL EP
+//      article, hotelren.com, §3.3: running sums of the send counts); CTA 0
+//      writes the layout outputs; each CTA writes its own pairs' rows
+//      (slot_row / row_slot).
+//   -- grid barrier 2 (not for small batches): every pair's row is written --
+//   C  scatter the payload: bf16 copies (a warp per token) or the per-token
+//      int8 / FP8 / int4 code (ThunderEP §2.3; a group of warps per token with
+//      its own named barrier). Small batches: each CTA its own tile, x from
+//      shared memory. Otherwise every group of every CTA takes the batch's
+//      tokens in order from one shared counter, so that the SMs, which move
+//      data at different speeds, and the tokens, whose kept rows differ
+//      (capacity drops fall on the later ones), even out.
 //
 // Every output equals that of route_count_kernel + scan_kernel + the scatter
 // kernels, bit for bit (the same routing, the same row rule, the same codes).
@@ -60,8 +61,10 @@ struct FusedArgs {
   const float* logits;
   const void* x;
   int T, H, E, k, R, cap, renorm, lanes_log2;
-  int tile, TW, npre, own_tile, small_layout;  // tokens per tile, mask words per expert (pow2), preloaded rows per CTA,
-                                // 1 when the preloaded rows are the CTA's own tile
+  int tile, TW;        // tokens per tile, mask words per expert (a power of two)
+  int npre;            // x rows preloaded per CTA (its own tile's), 0 for none
+  int own_tile;        // 1: each CTA scatters its own tile (no second barrier)
+  int small_layout;    // 1: the layout comes from the routed ids, not the tile counts
   int32_t* topk_idx;
   float* topk_w;
   void* payload;

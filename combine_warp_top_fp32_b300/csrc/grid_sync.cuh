@@ -38,10 +38,6 @@ __device__ __forceinline__ void red_add_release_gpu(unsigned* p, unsigned v) {
   asm volatile("red.add.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 
-__device__ __forceinline__ void st_release_gpu(unsigned* p, unsigned v) {
-  asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
-}
-
 // All threads of the CTA call it. Returns true once every one of `expected`
 // CTAs has arrived (their writes before the barrier are then visible to every
 // thread of this CTA), false if thread 0 gave up after `limit` polls. The
@@ -49,18 +45,13 @@ __device__ __forceinline__ void st_release_gpu(unsigned* p, unsigned v) {
 // a release and its wait an acquire at GPU scope. The last CTA to arrive
 // also stores `reset_value` to `*reset` (when given) before it lets the others
 // go, so a counter used after the barrier starts from a known value.
-// *round_after (when given) receives the round the barrier completes: the
-// same in every CTA, and different in consecutive uses of the words.
 __device__ __forceinline__ bool grid_barrier(GridBarrier bar, unsigned expected, long long limit,
-                                             unsigned* reset = nullptr, unsigned reset_value = 0u,
-                                             unsigned* round_after = nullptr) {
+                                             unsigned* reset = nullptr, unsigned reset_value = 0u) {
   __shared__ int passed_s;
-  __shared__ unsigned round_s;
   __syncthreads();
   if (threadIdx.x == 0) {
     int passed = 1;
     const unsigned r = ld_acquire_gpu(bar.round);
-    round_s = r + 1u;
     const unsigned prev = atom_add_acq_rel_gpu(bar.count, 1u);
     if (prev == expected - 1) {
       *reinterpret_cast<volatile unsigned*>(bar.count) = 0u;
@@ -79,7 +70,6 @@ __device__ __forceinline__ bool grid_barrier(GridBarrier bar, unsigned expected,
     passed_s = passed;
   }
   __syncthreads();
-  if (round_after) *round_after = round_s;
   return passed_s != 0;
 }
 

@@ -49,6 +49,10 @@ def test_bench_line_on_decode_latency(monkeypatch):
     assert e2e["value"] > 0 and e2e["unit"] == "tokens/s"
     assert e2e["h2d_bytes_per_step"] == w.T * w.E * 4 + w.T * w.H * 2  # logits + x
     assert e2e["d2h_bytes_per_step"] == w.T * w.H * 2  # y
+    link = e2e["link"]  # the host link's own bound, measured in the same run
+    assert link["h2d_gbs"] > 0 and link["d2h_gbs"] > 0 and link["both_ms"] > 0
+    assert link["bound_ms_per_step"] == pytest.approx(max(link["both_ms"], d["ms_per_step"]))
+    assert 0 < link["frac_of_bound"] <= 1.05
 
     both = d["int8_both_directions"]
     assert both["value"] > 0 and both["bytes_per_step"] < d["hbm"]["bytes_per_step"]
