@@ -38,6 +38,24 @@ EXPORTS = (
 )
 
 
+def _header_constant(name: str) -> int:
+    """An integer #define of include/ep.h (an expression of integer literals)."""
+    import re
+
+    text = (_PKG.parent / "include" / "ep.h").read_text()
+    m = re.search(rf"#define\s+{name}\s+\(([0-9u*+ ]+)\)", text)
+    if m is None:
+        raise ImportError(f"{name} not found in include/ep.h")
+    value = 1
+    for factor in m.group(1).replace("u", "").split("*"):
+        value *= int(factor)
+    return value
+
+
+# Size of ep_dispatch_static's fixed scratch array.
+EP_STATIC_SCRATCH_BYTES = _header_constant("EP_STATIC_SCRATCH_BYTES")
+
+
 class EpError(RuntimeError):
     def __init__(self, status: int, where: str):
         self.status = status

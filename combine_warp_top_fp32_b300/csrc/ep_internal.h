@@ -117,7 +117,10 @@ inline cudaError_t launch_pdl(void (*kernel)(KArgs...), int grid, int block, siz
 // e.g. when the process is limited to a share of the SMs) is asked once per
 // device and cluster size and kept in `fits` (0 unknown, 1 yes, -1 no); if it
 // cannot, nothing is launched and cudaErrorNotSupported is returned, so that
-// the caller can take its general path.
+// the caller can take its general path. Only an answer is kept: a query that
+// fails is asked again next time. The key leaves out the dynamic shared
+// memory, which for the one kernel launched this way is at most 11 KB (E <= 256
+// experts, 8 tiles), far below what decides residency.
 constexpr int kMaxCluster = 8;  // the portable cluster size
 using ClusterFits = signed char[64][kMaxCluster + 1];
 template <typename... KArgs, typename... Args>
@@ -146,8 +149,8 @@ inline cudaError_t launch_cluster_pdl(void (*kernel)(KArgs...), int grid, int bl
     int clusters = 0;
     err = cudaOccupancyMaxActiveClusters(&clusters, kernel, &cfg);
     if (err != cudaSuccess) {
-      (void)cudaGetLastError();  // a refused query is not an error of this call
-      clusters = 0;
+      (void)cudaGetLastError();  // a refused query is not an error of this call: take the general path
+      return cudaErrorNotSupported;
     }
     f = clusters > 0 ? 1 : -1;
     if (dev < 64) cache_store(&fits[dev][grid], f);
