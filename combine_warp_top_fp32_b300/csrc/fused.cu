@@ -42,7 +42,7 @@ namespace {
 
 using namespace routing;
 
-constexpr int kFusedBlock = 1024;       // 32 warps: a whole SM per CTA
+constexpr int kFusedBlock = 768;  // one CTA per SM; 24 warps leave 85 registers a thread, so neither phase spills
 constexpr int kFusedMaxGroups = 15;     // named barriers 1..15: at most 15 token groups
 constexpr long long kBarrierPolls = 1ll << 20;  // about a second of polling before a wait gives up
 constexpr long long kCopyPolls = 1ll << 22;
@@ -167,7 +167,7 @@ __device__ __forceinline__ void tile_bases(const int32_t* __restrict__ counts, i
     int4 bf[2] = {make_int4(0, 0, 0, 0), make_int4(0, 0, 0, 0)};
     int4 tt[2] = {make_int4(0, 0, 0, 0), make_int4(0, 0, 0, 0)};
     if (C4 <= 32) {  // E <= 128: one int4 per lane per row, all of a warp's rows in flight at once
-      constexpr int RW = kFusedMaxCTAs / NW;
+      constexpr int RW = (kFusedMaxCTAs + NW - 1) / NW;
       int4 v[RW];
 #pragma unroll
       for (int r = 0; r < RW; ++r) {
@@ -452,7 +452,7 @@ __global__ void __launch_bounds__(kFusedBlock, 1) route_dispatch_fused_kernel(co
     // rows two tokens ahead, so that no exchange waits for a load.
     const int ngrp16 = a.H >> 4;
     const int gw = (((ngrp16 + 1) >> 1) + 31) >> 5;  // warps per token
-    const int ngroups = min(32 / gw, kFusedMaxGroups);
+    const int ngroups = min((kFusedBlock / 32) / gw, kFusedMaxGroups);
     const int g = warp / gw;
     if (g < ngroups) {
       const int gsz = gw * 32;
@@ -532,23 +532,32 @@ __global__ void __launch_bounds__(kFusedBlock, 1) route_dispatch_fused_kernel(co
         const float scale = __fdiv_rn(am, CodeMax<FMT>::kValue);
         const float inv = __frcp_rn(scale);
         const int32_t* rows = rows_s[g][rb];
-#pragma unroll
-        for (int q = 0; q < 2; ++q) {
-          const int grp = c + q * gsz;
-          if (grp >= ngrp16) break;
+        // both of this thread's groups coded first, then one pass over the
+        // kept rows, each row's address formed once
+        const int grp0 = c, grp1 = c + gsz;
+        const bool has1 = grp1 < ngrp16;
+        if (grp0 < ngrp16) {
           if constexpr (FMT == kFmtInt4) {
-            const uint2 qv = quant16_int4_coded(cur[2 * q], cur[2 * q + 1], scale, inv);
+            const uint2 q0 = quant16_int4_coded(cur[0], cur[1], scale, inv);
+            const uint2 q1 = has1 ? quant16_int4_coded(cur[2], cur[3], scale, inv) : make_uint2(0, 0);
+            char* const pb = static_cast<char*>(a.payload);
             for (int j = 0; j < a.k; ++j) {
               const int row = rows[j];
-              if (row >= 0)
-                st_v2_hint(static_cast<char*>(a.payload) + static_cast<int64_t>(row) * (a.H / 2) + 8 * grp, qv, pol);
+              if (row < 0) continue;
+              char* dst = pb + static_cast<int64_t>(row) * (a.H / 2);
+              st_v2_hint(dst + 8 * grp0, q0, pol);
+              if (has1) st_v2_hint(dst + 8 * grp1, q1, pol);
             }
           } else {
-            const uint4 qv = quant16_fmt<FMT>(cur[2 * q], cur[2 * q + 1], scale, inv);
+            const uint4 q0 = quant16_fmt<FMT>(cur[0], cur[1], scale, inv);
+            const uint4 q1 = has1 ? quant16_fmt<FMT>(cur[2], cur[3], scale, inv) : make_uint4(0, 0, 0, 0);
+            char* const pb = static_cast<char*>(a.payload);
             for (int j = 0; j < a.k; ++j) {
               const int row = rows[j];
-              if (row >= 0)
-                st_v4_hint(static_cast<int8_t*>(a.payload) + static_cast<int64_t>(row) * a.H + 16 * grp, qv, pol);
+              if (row < 0) continue;
+              char* dst = pb + static_cast<int64_t>(row) * a.H;
+              st_v4_hint(dst + 16 * grp0, q0, pol);
+              if (has1) st_v4_hint(dst + 16 * grp1, q1, pol);
             }
           }
         }

@@ -37,7 +37,10 @@ __global__ void __launch_bounds__(256) route_topk_kernel(const float* __restrict
         const bool act[2] = {true, tb + n_warps < T};
         int e[2];
         float w[2];
-        route_tokens_sorted<2, VPL, VEC4>(logits, tq, act, E, k, lane, renorm, e, w);
+        if (k <= 8)
+          route_tokens_sorted<2, VPL, VEC4, 8>(logits, tq, act, E, k, lane, renorm, e, w);
+        else
+          route_tokens_sorted<2, VPL, VEC4, 0>(logits, tq, act, E, k, lane, renorm, e, w);
 #pragma unroll
         for (int q = 0; q < 2; ++q)
           if (act[q] && lane < k) {

@@ -115,6 +115,35 @@ __device__ __forceinline__ float exp_shifted_term(float v, float m) {
   return __fmaf_rn(r, __fmul_rn(c, kLn2), r);
 }
 
+// exp_shifted_term of both halves of v2 at once (nm2 = -m in both halves),
+// with packed f32x2 operations: each is the IEEE operation of the scalar form
+// on each half (p is formed negated, pn = fl(d * -log2e_hi) = -fl(d * log2e_hi)
+// exactly), so the two results equal exp_shifted_term's bit for bit.
+__device__ __forceinline__ uint64_t exp_shifted_term2(uint64_t v2, uint64_t nm2) {
+  constexpr float kLog2eHi = 1.44269502162933349609375f;
+  constexpr float kLog2eLo = 1.925963033500011e-08f;
+  constexpr float kLn2 = 0.693147180559945309f;
+  const uint64_t d = f32x2_add(v2, nm2);
+  const uint64_t bb = f32x2_sub(d, v2);
+  const uint64_t err = f32x2_add(f32x2_sub(v2, f32x2_sub(d, bb)), f32x2_sub(nm2, bb));
+  const uint64_t pn = f32x2_mul(d, f32x2_splat(-kLog2eHi));
+  const uint64_t c = f32x2_fma(err, f32x2_splat(kLog2eHi),
+                               f32x2_fma(d, f32x2_splat(kLog2eLo), f32x2_fma(d, f32x2_splat(kLog2eHi), pn)));
+  float r0, r1;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(r0) : "f"(-f32x2_lo(pn)));
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(r1) : "f"(-f32x2_hi(pn)));
+  const uint64_t r = f32x2_pack(__float_as_uint(r0), __float_as_uint(r1));
+  return f32x2_fma(r, f32x2_mul(c, f32x2_splat(kLn2)), r);
+}
+
+// comp_add on both halves of (s, c) at once.
+__device__ __forceinline__ void comp_add2(uint64_t& s, uint64_t& c, uint64_t x) {
+  const uint64_t t = f32x2_add(s, x);
+  const uint64_t bb = f32x2_sub(t, s);
+  c = f32x2_add(c, f32x2_add(f32x2_sub(s, f32x2_sub(t, bb)), f32x2_sub(x, bb)));
+  s = t;
+}
+
 // Compensated accumulation of x into (s, c): TwoSum gives the exact rounding
 // error of s + x, which is added to the running correction c.
 __device__ __forceinline__ void comp_add(float& s, float& c, float x) {
@@ -282,11 +311,16 @@ __device__ __forceinline__ void route_token(const float* __restrict__ logits, in
 
 // NQ tokens per warp at once (one token per 32 lanes, E >= 32, at most 8
 // values per lane; the kernels use NQ = 2 up to 4 values per lane, where the
-// doubled registers still leave room for many warps): the same steps as route_token on the sorted-key path, with
-// every per-token value held for all NQ tokens so that the NQ independent
-// chains of reductions and exponentials interleave in one warp. On return lane
-// j < k holds slot j of token q in e_out[q] / w_out[q].
-template <int NQ, int VPL, bool VEC4>
+// doubled registers still leave room for many warps): the same steps as
+// route_token on the sorted-key path, with every per-token value held for all
+// NQ tokens so that the NQ independent chains of reductions and exponentials
+// interleave in one warp. KMAX > 0: the top-k rounds are unrolled for
+// k <= KMAX (the round index is then a constant in each copy); 0: a loop.
+// With an even number of values per lane the softmax denominator takes its
+// terms two at a time in packed f32x2 arithmetic (two interleaved compensated
+// sums per lane, merged before the butterfly). On return lane j < k holds
+// slot j of token q in e_out[q] / w_out[q].
+template <int NQ, int VPL, bool VEC4, int KMAX>
 __device__ __forceinline__ void route_tokens_sorted(const float* __restrict__ logits, const int64_t (&t)[NQ],
                                                     const bool (&active)[NQ], int E, int k, int lane, int renorm,
                                                     int (&e_out)[NQ], float (&w_out)[NQ]) {
@@ -328,7 +362,7 @@ __device__ __forceinline__ void route_tokens_sorted(const float* __restrict__ lo
     max_bits[q] = 0u;
     e_out[q] = 0;
   }
-  for (int r = 0; r < k; ++r) {
+  auto round = [&](int r) {
     uint32_t gmax[NQ], cand[NQ], win[NQ];
 #pragma unroll
     for (int q = 0; q < NQ; ++q) gmax[q] = __reduce_max_sync(0xffffffffu, static_cast<uint32_t>(key[q][0] >> 32));
@@ -351,6 +385,15 @@ __device__ __forceinline__ void route_tokens_sorted(const float* __restrict__ lo
         key[q][VPL - 1] = 0ull;  // 0 is below every real key
       }
     }
+  };
+  if constexpr (KMAX > 0) {
+#pragma unroll
+    for (int r = 0; r < KMAX; ++r) {
+      if (r >= k) break;
+      round(r);
+    }
+  } else {
+    for (int r = 0; r < k; ++r) round(r);
   }
 
   float l_max[NQ], my_v[NQ], s[NQ], c[NQ];
@@ -365,6 +408,28 @@ __device__ __forceinline__ void route_tokens_sorted(const float* __restrict__ lo
 #pragma unroll
     for (int q = 0; q < NQ; ++q)
       if (lane < k) s[q] = exp_shifted_term(my_v[q], l_max[q]);
+  } else if constexpr (VPL % 2 == 0) {
+#pragma unroll
+    for (int q = 0; q < NQ; ++q) {
+      const uint64_t nm2 = f32x2_splat(-l_max[q]);
+      uint64_t s2 = 0ull, c2 = 0ull;
+#pragma unroll
+      for (int i = 0; i < VPL; i += 2) {
+        uint64_t term = exp_shifted_term2(f32x2_pack(__float_as_uint(val[q][i]), __float_as_uint(val[q][i + 1])), nm2);
+        // a value that is not an expert's adds +0, which leaves (s, c) as they were
+        const bool ok0 = VEC4 ? active[q] : (active[q] && (lane + 32 * i) < E);
+        const bool ok1 = VEC4 ? active[q] : (active[q] && (lane + 32 * (i + 1)) < E);
+        term &= (ok0 ? 0x00000000ffffffffull : 0ull) | (ok1 ? 0xffffffff00000000ull : 0ull);
+        comp_add2(s2, c2, term);
+      }
+      // the lane's two compensated sums, merged as the butterfly merges lanes
+      const float sa = f32x2_lo(s2), sb = f32x2_hi(s2);
+      const float tt = __fadd_rn(sa, sb);
+      const float bb = __fsub_rn(tt, sa);
+      const float err = __fadd_rn(__fsub_rn(sa, __fsub_rn(tt, bb)), __fsub_rn(sb, bb));
+      c[q] = __fadd_rn(__fadd_rn(f32x2_lo(c2), f32x2_hi(c2)), err);
+      s[q] = tt;
+    }
   } else {
 #pragma unroll
     for (int i = 0; i < VPL; ++i)
@@ -415,7 +480,10 @@ __device__ __forceinline__ void route_tile(const float* __restrict__ logits, int
         const bool act[2] = {true, tl0 + nw < nt};
         int e[2];
         float w[2];
-        route_tokens_sorted<2, VPL, VEC4>(logits, tq, act, E, k, lane, renorm, e, w);
+        if (k <= 8)
+          route_tokens_sorted<2, VPL, VEC4, 8>(logits, tq, act, E, k, lane, renorm, e, w);
+        else
+          route_tokens_sorted<2, VPL, VEC4, 0>(logits, tq, act, E, k, lane, renorm, e, w);
 #pragma unroll
         for (int q = 0; q < 2; ++q)
           if (act[q] && lane < k) {
