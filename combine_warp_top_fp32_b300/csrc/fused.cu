@@ -46,6 +46,15 @@ constexpr int kFusedBlock = 768;  // one CTA per SM; 24 warps leave 85 registers
 constexpr int kFusedMaxGroups = 15;     // named barriers 1..15: at most 15 token groups
 constexpr long long kBarrierPolls = 1ll << 20;  // about a second of polling before a wait gives up
 constexpr long long kCopyPolls = 1ll << 22;
+// The scatter's own part is kOwnPerGroup tokens for each token group of the
+// CTA in the coded scatter and kOwnPerWarp for each warp in the bf16 one (at
+// most the tile): enough work that a group rarely finds the second grid
+// barrier incomplete (every group's first thread polls it then), and little
+// enough on large tiles that the shared part, whose concurrent tokens are
+// neighbours in the batch (so are the payload rows they write), does most
+// of the work.
+constexpr int kOwnPerGroup = 8;
+constexpr int kOwnPerWarp = 4;
 // x rows are preloaded into shared memory only when a whole tile's rows fit in
 // kPreloadBytes (small batches: each CTA then scatters exactly its own tile,
 // with no wait on any other CTA). Otherwise nothing is preloaded: the SM's
@@ -73,7 +82,7 @@ struct FusedArgs {
   int32_t* counts;  // workspace: [G][E] per-tile counts
   uint32_t* status;
   GridBarrier bar;
-  unsigned* work;  // the scatter's token counter, zeroed at the first grid barrier
+  unsigned* work;  // the scatter's shared token counter, zeroed at the first grid barrier
   int extra_arrivals;  // > 0 only when a test forces the barrier to time out
   long long barrier_polls;
 };
@@ -237,6 +246,59 @@ __device__ __forceinline__ void tile_bases(const int32_t* __restrict__ counts, i
   }
 }
 
+// The scatter's tokens, in two parts. Own part: the first `own` tokens of
+// each tile (the same number in every tile), scattered by the tile's CTA
+// straight after it has written its rows, its groups (warps) taking them in
+// turn: no atomic, and no wait on any other CTA. Shared part: the rest of
+// every tile, handed out by one counter to every group of every CTA (so that
+// SMs that run faster, and tiles with fewer kept rows, even out: capacity
+// drops fall on the batch's later tokens). A group takes from the counter
+// only after the second grid barrier, which each CTA arrives at when its rows
+// are written and waits for only once its own part is done, by when the
+// barrier has normally completed. Counter value p is token
+// (p / (tile - own)) * tile + own + p % (tile - own); values past the batch
+// end the sequence. A value is asked for (issue) one token before it is read
+// (resolve), so no group waits on the atomic. One thread per group calls
+// these.
+struct TokenPlan {
+  unsigned* work;           // the shared counter (zeroed at the first grid barrier)
+  const unsigned* round;    // the grid barrier's round word
+  uint32_t* status;
+  unsigned round_before;    // the round while the second barrier is incomplete
+  int T, tile, own, t0, own_end;
+};
+
+// ticket >= 0: a token of the own part; < 0: -(counter value + 1).
+__device__ __forceinline__ int plan_issue(const TokenPlan& tp, int& own_next, int step, bool& shared_ok) {
+  if (own_next < tp.own_end) {
+    const int t = own_next;
+    own_next += step;
+    return t;
+  }
+  if (tp.own >= tp.tile) return -1;  // own-tile mode: no shared part (resolves past the batch)
+  if (!shared_ok) {  // the second barrier: every tile's rows are written
+    long long polls = 0;
+    while (ld_acquire_gpu(tp.round) == tp.round_before) {
+      if (++polls > kBarrierPolls) {
+        raise_status(tp.status, kStatusTimeout);
+        return -1 - 0x3fffffff;  // past every token: ends the sequence
+      }
+      __nanosleep(16);
+    }
+    shared_ok = true;
+  }
+  return -1 - static_cast<int>(atomicAdd(tp.work, 1u));
+}
+
+__device__ __forceinline__ int plan_resolve(const TokenPlan& tp, int ticket) {
+  if (ticket >= 0) return ticket;
+  const int p = -1 - ticket;
+  const int per = tp.tile - tp.own;
+  if (per <= 0) return tp.T;
+  const int64_t t = static_cast<int64_t>(p / per) * tp.tile + tp.own + p % per;
+  return t < tp.T ? static_cast<int>(t) : tp.T;
+}
+
 template <int VPL, bool VEC4, int FMT>
 __global__ void __launch_bounds__(kFusedBlock, 1) route_dispatch_fused_kernel(const FusedArgs a) {
   extern __shared__ __align__(128) unsigned char smem_raw[];
@@ -278,7 +340,8 @@ __global__ void __launch_bounds__(kFusedBlock, 1) route_dispatch_fused_kernel(co
   __syncthreads();
   tile_word_prefix_row(s.mask, s.pre, a.E, a.TW, a.counts + static_cast<int64_t>(b) * a.E);
 
-  bool ok = grid_barrier(a.bar, static_cast<unsigned>(G + a.extra_arrivals), a.barrier_polls, a.work, 0u);
+  unsigned round = 0u;
+  bool ok = grid_barrier(a.bar, static_cast<unsigned>(G + a.extra_arrivals), a.barrier_polls, a.work, 0u, &round);
 
   if (ok) {
     // ---- B: this tile's first position within each expert, the offsets ------
@@ -344,10 +407,10 @@ __global__ void __launch_bounds__(kFusedBlock, 1) route_dispatch_fused_kernel(co
       const int tl = p / a.k;
       fused_row(a, s, t0 + tl, tl, p - tl * a.k);
     }
-    // every tile's rows are written before any CTA scatters another tile's
-    // tokens; a CTA that scatters only its own tile needs just its own barrier
-    if (!own_tile) ok = grid_barrier(a.bar, static_cast<unsigned>(G + a.extra_arrivals), a.barrier_polls);
-    else __syncthreads();
+    // this tile's rows are written: arrive at the second grid barrier (its
+    // wait comes when the own part is done)
+    __syncthreads();
+    if (tid == 0 && !own_tile) grid_arrive(a.bar, static_cast<unsigned>(G + a.extra_arrivals));
   }
   if (!ok) {
     if (tid == 0) {
@@ -358,12 +421,11 @@ __global__ void __launch_bounds__(kFusedBlock, 1) route_dispatch_fused_kernel(co
   }
 
   // ---- C: scatter -------------------------------------------------------------------
-  // Own-tile mode: the CTA scatters its own tile (x preloaded in shared
-  // memory), its groups (or warps) taking tokens t0 + g, t0 + g + n, ...
-  // Otherwise the groups (warps) of every CTA take the batch's tokens in
-  // order from one shared counter, so that SMs that run faster, and tokens
-  // with fewer kept rows, even out. Each counter value is asked for two
-  // tokens before it is needed, so that no group waits on the atomic.
+  // The groups (or warps) of the CTA take tokens t0 + g, t0 + g + n, ... of
+  // its own tile's first part, then the rest of every tile from the shared
+  // counter once the second barrier has completed (TokenPlan). Own-tile mode:
+  // the whole tile is the first part (x preloaded in shared memory) and
+  // nothing is shared.
   const uint64_t pol = l2_evict_first_policy();  // x and payload lines: first out of L2
   auto x_src = [&](int t) -> const char* {  // a token's x row: shared memory for the preloaded tail
     if (t >= tail0 && t < tail0 + P) return reinterpret_cast<const char*>(s.xpre) + (t - tail0) * row_bytes;
@@ -377,27 +439,26 @@ __global__ void __launch_bounds__(kFusedBlock, 1) route_dispatch_fused_kernel(co
     constexpr int U = 8;
     char* const pbase = static_cast<char*>(a.payload);
     const int nchunk = a.H >> 3;
-    const int end = own_tile ? static_cast<int>(t0) + nt : a.T;
-    // the token sequence of this warp: own tile, or the shared counter (lane 0)
+    const int end = a.T;
+    // the token sequence of this warp (lane 0): its share of the own part,
+    // then the shared part (own-tile mode: the whole tile is the own part)
+    const int own = own_tile ? a.tile : min(a.tile, kOwnPerWarp * (kFusedBlock / 32));
+    const TokenPlan tp{a.work, a.bar.round, a.status, round, a.T, a.tile, own, static_cast<int>(t0),
+                       static_cast<int>(t0) + min(nt, own)};
     int own_next = static_cast<int>(t0) + warp;
-    auto take = [&]() -> int {
-      if (own_tile) {
-        const int t = own_next;
-        own_next += kFusedBlock / 32;
-        return t;
-      }
-      return lane == 0 ? static_cast<int>(atomicAdd(a.work, 1u)) : 0;
-    };
+    bool shared_ok = false;
+    auto issue = [&]() -> int { return lane == 0 ? plan_issue(tp, own_next, kFusedBlock / 32, shared_ok) : 0; };
+    auto resolve = [&](int ticket) -> int { return lane == 0 ? plan_resolve(tp, ticket) : 0; };
     auto slot_rows = [&](int tok) {
       return tok < end && lane < a.k ? __ldcg(a.slot_row + static_cast<int64_t>(tok) * a.k + lane) : -1;
     };
-    int t = __shfl_sync(0xffffffffu, take(), 0);
-    int tn = __shfl_sync(0xffffffffu, take(), 0);
-    int pend = take();  // the token after next: read one token later
+    int t = __shfl_sync(0xffffffffu, resolve(issue()), 0);
+    int tn = __shfl_sync(0xffffffffu, resolve(issue()), 0);
+    int pend = issue();  // the ticket of the token after next: read one token later
     int row = slot_rows(t), row_n = slot_rows(tn);  // this token's and the next token's rows
     while (t < end) {
-      const int tnn = __shfl_sync(0xffffffffu, pend, 0);
-      pend = tnn < end ? take() : end;
+      const int tnn = __shfl_sync(0xffffffffu, tn < end ? resolve(pend) : end, 0);
+      pend = tnn < end ? issue() : 0;
       const int row_nn = slot_rows(tnn);  // in flight for two tokens
       const unsigned kept = __ballot_sync(0xffffffffu, row >= 0);
       if (kept != 0u) {
@@ -464,17 +525,16 @@ __global__ void __launch_bounds__(kFusedBlock, 1) route_dispatch_fused_kernel(co
         else
           group_sync(1 + g, gsz);
       };
-      const int end = own_tile ? static_cast<int>(t0) + nt : a.T;
-      // the group's token sequence: own tile, or the shared counter (thread 0)
+      const int end = a.T;
+      // the group's token sequence (thread 0): its share of the own part,
+      // then the shared part (own-tile mode: the whole tile is the own part)
+      const int own = own_tile ? a.tile : min(a.tile, kOwnPerGroup * ngroups);
+      const TokenPlan tp{a.work, a.bar.round, a.status, round, a.T, a.tile, own, static_cast<int>(t0),
+                         static_cast<int>(t0) + min(nt, own)};
       int own_next = static_cast<int>(t0) + g;
-      auto take = [&]() -> int {
-        if (own_tile) {
-          const int t = own_next;
-          own_next += ngroups;
-          return t;
-        }
-        return static_cast<int>(atomicAdd(a.work, 1u));
-      };
+      bool shared_ok = false;
+      auto issue = [&]() -> int { return plan_issue(tp, own_next, ngroups, shared_ok); };
+      auto resolve = [&](int ticket) -> int { return plan_resolve(tp, ticket); };
       auto load_x = [&](int t, uint4 (&v)[4]) {  // this thread's 32 elements of token t's row
         const char* sx = x_src(t);
         if (sx) wait_pre();
@@ -500,9 +560,9 @@ __global__ void __launch_bounds__(kFusedBlock, 1) route_dispatch_fused_kernel(co
       };
       int pend = 0;
       if (c == 0) {
-        ids_s[g][0] = take();
-        ids_s[g][1] = take();
-        pend = take();  // the token after next: published at the next exchange
+        ids_s[g][0] = resolve(issue());
+        ids_s[g][1] = ids_s[g][0] < end ? resolve(issue()) : end;
+        pend = ids_s[g][1] < end ? issue() : 0;  // the ticket after next: read at the next exchange
       }
       gsync();
       int t = ids_s[g][0], tn = ids_s[g][1];
@@ -518,8 +578,9 @@ __global__ void __launch_bounds__(kFusedBlock, 1) route_dispatch_fused_kernel(co
         if (tn < end) load_x(tn, nxt);  // in flight while this token is coded
         if (c < a.k) rows_s[g][rbn][c] = r_n;
         if (c == 0) {
-          ids_s[g][ab] = pend;
-          pend = pend < end ? take() : end;  // read at the next exchange
+          const int tnn = tn < end ? resolve(pend) : end;
+          ids_s[g][ab] = tnn;
+          pend = tnn < end ? issue() : 0;  // read at the next exchange
         }
         float m = fmaxf(absmax_bf16x16(cur[0], cur[1]), absmax_bf16x16(cur[2], cur[3]));
         m = warp_max(m);

@@ -45,13 +45,18 @@ __device__ __forceinline__ void red_add_release_gpu(unsigned* p, unsigned v) {
 // a release and its wait an acquire at GPU scope. The last CTA to arrive
 // also stores `reset_value` to `*reset` (when given) before it lets the others
 // go, so a counter used after the barrier starts from a known value.
+// *round_after (when given) receives the round the barrier completes: the
+// same in every CTA, and different in consecutive uses of the words.
 __device__ __forceinline__ bool grid_barrier(GridBarrier bar, unsigned expected, long long limit,
-                                             unsigned* reset = nullptr, unsigned reset_value = 0u) {
+                                             unsigned* reset = nullptr, unsigned reset_value = 0u,
+                                             unsigned* round_after = nullptr) {
   __shared__ int passed_s;
+  __shared__ unsigned round_s;
   __syncthreads();
   if (threadIdx.x == 0) {
     int passed = 1;
     const unsigned r = ld_acquire_gpu(bar.round);
+    round_s = r + 1u;
     const unsigned prev = atom_add_acq_rel_gpu(bar.count, 1u);
     if (prev == expected - 1) {
       *reinterpret_cast<volatile unsigned*>(bar.count) = 0u;
@@ -70,7 +75,21 @@ __device__ __forceinline__ bool grid_barrier(GridBarrier bar, unsigned expected,
     passed_s = passed;
   }
   __syncthreads();
+  if (round_after) *round_after = round_s;
   return passed_s != 0;
+}
+
+// The arrival half of a split grid barrier, by one thread after a CTA
+// barrier (so the CTA's writes before it are ordered before the arrival): the
+// last of `expected` CTAs to arrive zeroes the arrivals and advances the round.
+// The wait half is a bounded poll until the round differs from the one seen at
+// the barrier before (every CTA knows it).
+__device__ __forceinline__ void grid_arrive(GridBarrier bar, unsigned expected) {
+  const unsigned prev = atom_add_acq_rel_gpu(bar.count, 1u);
+  if (prev == expected - 1) {
+    *reinterpret_cast<volatile unsigned*>(bar.count) = 0u;
+    red_add_release_gpu(bar.round, 1u);
+  }
 }
 
 // ---- mbarrier + 1-D bulk copy (global -> this CTA's shared memory) ----------

@@ -30,24 +30,14 @@ __global__ void __launch_bounds__(256) route_topk_kernel(const float* __restrict
   pdl_wait();  // the logits may come from the kernel before this one
   pdl_launch_dependents();
 
-  if constexpr (VPL <= 4) {
-    if (L == 32) {  // two tokens per warp in flight: tokens w and w + n_warps
-      for (int64_t tb = warp_id; tb < T; tb += 2 * n_warps) {
-        const int64_t tq[2] = {tb, tb + n_warps};
-        const bool act[2] = {true, tb + n_warps < T};
-        int e[2];
-        float w[2];
-        if (k <= 8)
-          route_tokens_sorted<2, VPL, VEC4, 8>(logits, tq, act, E, k, lane, renorm, e, w);
-        else
-          route_tokens_sorted<2, VPL, VEC4, 0>(logits, tq, act, E, k, lane, renorm, e, w);
-#pragma unroll
-        for (int q = 0; q < 2; ++q)
-          if (act[q] && lane < k) {
-            topk_idx[tq[q] * k + lane] = e[q];
-            topk_w[tq[q] * k + lane] = w[q];
-          }
-      }
+  if constexpr (VPL <= 8) {
+    if (L == 32) {  // tokens w, w + n_warps, ...: NQ per warp at once, the next ones' logits loaded meanwhile
+      constexpr int NQ = VPL <= 4 ? 2 : 1;
+      route_warp<NQ, VPL, VEC4>(logits, 0, warp_id, NQ * n_warps, n_warps, T, E, k, lane, renorm,
+                                [&](int64_t, int64_t t, int e, float w) {
+                                  topk_idx[t * k + lane] = e;
+                                  topk_w[t * k + lane] = w;
+                                });
       return;
     }
   }

@@ -170,7 +170,9 @@ __device__ __forceinline__ float group_comp_sum(float s, float c, int L) {
 
 // Routes one token per L-lane group: on return lanes sub < k of the group
 // hold slot sub's expert id (*e_out) and weight (*w_out). All 32 lanes of the
-// warp must call it together (warp-wide reductions).
+// warp must call it together (warp-wide reductions). The kernels use it for
+// E < 32 (several tokens per warp) and for more than 8 values per lane
+// (E > 256); route_tokens_sorted covers the rest.
 template <int VPL, bool VEC4>
 __device__ __forceinline__ void route_token(const float* __restrict__ logits, int64_t t, bool active, int E, int k,
                                             int L, int sub, int renorm, int* e_out, float* w_out) {
@@ -207,33 +209,7 @@ __device__ __forceinline__ void route_token(const float* __restrict__ logits, in
   int my_e = 0;
   float my_v = 0.f;
   float l_max = 0.f;
-  if (L == 32 && VPL <= 8) {
-    // One token per warp, each lane's keys sorted once (largest first):
-    // every round the lanes offer their head key; redux.sync max over the
-    // value bits finds the largest logit, redux.sync min over the ids of
-    // the lanes offering it breaks the tie toward the lower expert id, and
-    // the winning lane drops its head (a shift of its sorted list).
-    sort_desc<VPL>(key);
-    uint32_t my_bits = 0, max_bits = 0;
-    for (int r = 0; r < k; ++r) {
-      const uint32_t hv = static_cast<uint32_t>(key[0] >> 32);
-      const uint32_t gmax = __reduce_max_sync(0xffffffffu, hv);
-      const uint32_t cand = (hv == gmax) ? 0xffffffffu - static_cast<uint32_t>(key[0]) : 0xffffffffu;
-      const uint32_t win = __reduce_min_sync(0xffffffffu, cand);
-      if (r == 0) max_bits = gmax;
-      if (sub == r) {
-        my_e = static_cast<int>(win);
-        my_bits = gmax;
-      }
-      if (cand == win) {
-#pragma unroll
-        for (int i = 0; i + 1 < VPL; ++i) key[i] = key[i + 1];
-        key[VPL - 1] = 0ull;  // 0 is below every real key
-      }
-    }
-    l_max = key_value(static_cast<uint64_t>(max_bits) << 32);
-    my_v = key_value(static_cast<uint64_t>(my_bits) << 32);
-  } else if (L == 32) {
+  if (L == 32) {
     // One token per warp: two single-instruction warp reductions per round.
     // redux.sync max over the order-preserving value bits finds the largest
     // logit, redux.sync min over the ids of the lanes holding it breaks the
@@ -309,47 +285,58 @@ __device__ __forceinline__ void route_token(const float* __restrict__ logits, in
   *w_out = __fdiv_rn(exp_shifted(my_v, l_max), denom);
 }
 
-// NQ tokens per warp at once (one token per 32 lanes, E >= 32, at most 8
-// values per lane; the kernels use NQ = 2 up to 4 values per lane, where the
-// doubled registers still leave room for many warps): the same steps as
-// route_token on the sorted-key path, with every per-token value held for all
-// NQ tokens so that the NQ independent chains of reductions and exponentials
-// interleave in one warp. KMAX > 0: the top-k rounds are unrolled for
-// k <= KMAX (the round index is then a constant in each copy); 0: a loop.
-// With an even number of values per lane the softmax denominator takes its
-// terms two at a time in packed f32x2 arithmetic (two interleaved compensated
-// sums per lane, merged before the butterfly). On return lane j < k holds
-// slot j of token q in e_out[q] / w_out[q].
-template <int NQ, int VPL, bool VEC4, int KMAX>
-__device__ __forceinline__ void route_tokens_sorted(const float* __restrict__ logits, const int64_t (&t)[NQ],
-                                                    const bool (&active)[NQ], int E, int k, int lane, int renorm,
-                                                    int (&e_out)[NQ], float (&w_out)[NQ]) {
-  float val[NQ][VPL];
-  uint64_t key[NQ][VPL];
+// The logits of NQ tokens (one per 32 lanes, E >= 32): lane `lane` gets
+// experts 4*lane + 128*i + c (VEC4: float4 loads) or lane + 32*i. Values of
+// inactive tokens and of ids >= E are 0 (their keys are cleared later).
+template <int NQ, int VPL, bool VEC4>
+__device__ __forceinline__ void load_logits(const float* __restrict__ logits, const int64_t (&t)[NQ],
+                                            const bool (&active)[NQ], int E, int lane, float (&val)[NQ][VPL]) {
 #pragma unroll
   for (int q = 0; q < NQ; ++q) {
     const float* row = logits + (active[q] ? t[q] : 0) * static_cast<int64_t>(E);
     if constexpr (VEC4) {
 #pragma unroll
       for (int i = 0; i < VPL / 4; ++i) {
-        const int e0 = 4 * lane + 128 * i;
         float4 f = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (active[q]) f = __ldg(reinterpret_cast<const float4*>(row + e0));
+        if (active[q]) f = __ldg(reinterpret_cast<const float4*>(row + 4 * lane + 128 * i));
         val[q][4 * i + 0] = f.x;
         val[q][4 * i + 1] = f.y;
         val[q][4 * i + 2] = f.z;
         val[q][4 * i + 3] = f.w;
-#pragma unroll
-        for (int c = 0; c < 4; ++c) key[q][4 * i + c] = active[q] ? make_key(val[q][4 * i + c], e0 + c) : 0ull;
       }
     } else {
 #pragma unroll
       for (int i = 0; i < VPL; ++i) {
         const int e = lane + 32 * i;
-        const bool ok = active[q] && e < E;
-        val[q][i] = ok ? __ldg(row + e) : 0.f;
-        key[q][i] = ok ? make_key(val[q][i], e) : 0ull;
+        val[q][i] = (active[q] && e < E) ? __ldg(row + e) : 0.f;
       }
+    }
+  }
+}
+
+// NQ tokens per warp at once (one token per 32 lanes, E >= 32, at most 8
+// values per lane, logits already in registers; the kernels use NQ = 2 up to
+// 4 values per lane, where the doubled registers still leave room for many
+// warps, and NQ = 1 above): the same steps as route_token on the sorted-key
+// path, with every per-token value held for all NQ tokens so that the NQ
+// independent chains of reductions and exponentials interleave in one warp.
+// KMAX > 0: the top-k rounds are unrolled for k <= KMAX (the round index is
+// then a constant in each copy); 0: a loop. With an even number of values per
+// lane the softmax denominator takes its terms two at a time in packed f32x2
+// arithmetic (two interleaved compensated sums per lane, merged before the
+// butterfly). On return lane j < k holds slot j of token q in e_out[q] /
+// w_out[q].
+template <int NQ, int VPL, bool VEC4, int KMAX>
+__device__ __forceinline__ void route_tokens_sorted(const float (&val)[NQ][VPL], const bool (&active)[NQ], int E,
+                                                    int k, int lane, int renorm, int (&e_out)[NQ],
+                                                    float (&w_out)[NQ]) {
+  uint64_t key[NQ][VPL];
+#pragma unroll
+  for (int q = 0; q < NQ; ++q) {
+#pragma unroll
+    for (int i = 0; i < VPL; ++i) {
+      const int e = VEC4 ? 4 * lane + 128 * (i / 4) + (i % 4) : lane + 32 * i;
+      key[q][i] = (active[q] && (VEC4 || e < E)) ? make_key(val[q][i], e) : 0ull;  // 0 is below every real key
     }
   }
 #pragma unroll
@@ -456,58 +443,93 @@ __device__ __forceinline__ void route_tokens_sorted(const float* __restrict__ lo
   for (int q = 0; q < NQ; ++q) w_out[q] = __fdiv_rn(exp_shifted(my_v[q], l_max[q]), __fadd_rn(s[q], c[q]));
 }
 
+// One warp routes tokens base + j for j = first + i*step + q*qstride (q < NQ,
+// i = 0, 1, ...) while j < end, NQ at a time, the next NQ tokens' logits
+// loaded while this NQ are routed (a warp otherwise waits a memory latency
+// per step). emit(j, t, e, w) is called by lanes < k of each routed token.
+template <int NQ, int VPL, bool VEC4, typename Emit>
+__device__ __forceinline__ void route_warp(const float* __restrict__ logits, int64_t base, int64_t first, int64_t step,
+                                           int64_t qstride, int64_t end, int E, int k, int lane, int renorm,
+                                           Emit&& emit) {
+  if (first >= end) return;
+  int64_t j[NQ], t[NQ];
+  bool act[NQ];
+  float cur[NQ][VPL];
+  auto locate = [&](int64_t j0, int64_t (&jj)[NQ], int64_t (&tt)[NQ], bool (&aa)[NQ]) {
+#pragma unroll
+    for (int q = 0; q < NQ; ++q) {
+      jj[q] = j0 + q * qstride;
+      aa[q] = jj[q] < end;
+      tt[q] = base + jj[q];
+    }
+  };
+  locate(first, j, t, act);
+  load_logits<NQ, VPL, VEC4>(logits, t, act, E, lane, cur);
+  for (int64_t j0 = first; j0 < end; j0 += step) {
+    int64_t jn[NQ], tn[NQ];
+    bool an[NQ];
+    float nxt[NQ][VPL];
+    locate(j0 + step, jn, tn, an);
+    load_logits<NQ, VPL, VEC4>(logits, tn, an, E, lane, nxt);  // in flight during this step
+    int e[NQ];
+    float w[NQ];
+    if (k <= 8)
+      route_tokens_sorted<NQ, VPL, VEC4, 8>(cur, act, E, k, lane, renorm, e, w);
+    else
+      route_tokens_sorted<NQ, VPL, VEC4, 0>(cur, act, E, k, lane, renorm, e, w);
+#pragma unroll
+    for (int q = 0; q < NQ; ++q)
+      if (act[q] && lane < k) emit(j[q], t[q], e[q], w[q]);
+#pragma unroll
+    for (int q = 0; q < NQ; ++q) {
+      j[q] = jn[q];
+      t[q] = tn[q];
+      act[q] = an[q];
+#pragma unroll
+      for (int i = 0; i < VPL; ++i) cur[q][i] = nxt[q][i];
+    }
+  }
+}
+
 // Routes the nt tokens of the tile starting at token t0 (one L-lane group
-// per token; two tokens per warp in flight when L = 32 and VPL <= 4), writes
-// their slots and sets their bits in the tile's per-expert masks in shared
-// memory: mask[e][w] bit b = token 32w+b of the tile chose e. The masks must
-// be zero on entry; the caller synchronises the CTA afterwards.
+// per token; with L = 32, two tokens per warp in flight up to 4 values per
+// lane and one above, the next ones' logits loaded meanwhile), writes their
+// slots and sets their bits in the tile's per-expert masks in shared memory:
+// mask[e][w] bit b = token 32w+b of the tile chose e. The masks must be zero
+// on entry; the caller synchronises the CTA afterwards.
 template <int VPL, bool VEC4>
 __device__ __forceinline__ void route_tile(const float* __restrict__ logits, int64_t t0, int nt, int E, int k,
                                            int lanes_log2, int renorm, int TW, uint32_t* mask,
                                            int32_t* __restrict__ topk_idx, float* __restrict__ topk_w) {
   const int L = 1 << lanes_log2;
   const int lane = threadIdx.x & 31;
+  const int warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  auto emit = [&](int64_t tl, int64_t t, int e, float w) {
+    topk_idx[t * k + lane] = e;
+    topk_w[t * k + lane] = w;
+    atomicOr(&mask[e * TW + static_cast<int>(tl >> 5)], 1u << (tl & 31));
+  };
+  if constexpr (VPL <= 8) {
+    if (L == 32) {
+      constexpr int NQ = VPL <= 4 ? 2 : 1;
+      route_warp<NQ, VPL, VEC4>(logits, t0, warp, NQ * nw, nw, nt, E, k, lane, renorm, emit);
+      return;
+    }
+  }
   const int sub = lane & (L - 1);
   const int groups_per_warp = 32 >> lanes_log2;
   const int grp = lane >> lanes_log2;
-  const int warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
-  bool routed = false;
-  if constexpr (VPL <= 4) {
-    if (L == 32) {  // two tokens per warp in flight: tile tokens w and w + nw
-      for (int tl0 = warp; tl0 < nt; tl0 += 2 * nw) {
-        const int tlq[2] = {tl0, tl0 + nw};
-        const int64_t tq[2] = {t0 + tl0, t0 + tl0 + nw};
-        const bool act[2] = {true, tl0 + nw < nt};
-        int e[2];
-        float w[2];
-        if (k <= 8)
-          route_tokens_sorted<2, VPL, VEC4, 8>(logits, tq, act, E, k, lane, renorm, e, w);
-        else
-          route_tokens_sorted<2, VPL, VEC4, 0>(logits, tq, act, E, k, lane, renorm, e, w);
-#pragma unroll
-        for (int q = 0; q < 2; ++q)
-          if (act[q] && lane < k) {
-            topk_idx[tq[q] * k + lane] = e[q];
-            topk_w[tq[q] * k + lane] = w[q];
-            atomicOr(&mask[e[q] * TW + (tlq[q] >> 5)], 1u << (tlq[q] & 31));
-          }
-      }
-      routed = true;
-    }
-  }
-  if (!routed) {
-    for (int tl0 = warp * groups_per_warp; tl0 < nt; tl0 += nw * groups_per_warp) {
-      const int tl = tl0 + grp;
-      const bool active = tl < nt;
-      const int64_t t = t0 + tl;
-      int e;
-      float w;
-      route_token<VPL, VEC4>(logits, t, active, E, k, L, sub, renorm, &e, &w);
-      if (active && sub < k) {
-        topk_idx[t * k + sub] = e;
-        topk_w[t * k + sub] = w;
-        atomicOr(&mask[e * TW + (tl >> 5)], 1u << (tl & 31));
-      }
+  for (int tl0 = warp * groups_per_warp; tl0 < nt; tl0 += nw * groups_per_warp) {
+    const int tl = tl0 + grp;
+    const bool active = tl < nt;
+    const int64_t t = t0 + tl;
+    int e;
+    float w;
+    route_token<VPL, VEC4>(logits, t, active, E, k, L, sub, renorm, &e, &w);
+    if (active && sub < k) {
+      topk_idx[t * k + sub] = e;
+      topk_w[t * k + sub] = w;
+      atomicOr(&mask[e * TW + (tl >> 5)], 1u << (tl & 31));
     }
   }
 }
