@@ -243,7 +243,10 @@ __global__ void __launch_bounds__(256, combine_min_ctas<FMT>()) combine_kernel(c
     if (nk <= 8) {
       unsigned m = kept;
       gather_group<FMT>(m, row, w, sc, base, row_bytes, p, wv, sv);
-      if (nk <= 2)
+      // coded rows: no separate 2-slot body (each body is long; fewer of
+      // them keep the instruction cache warm: int4 92 -> 74 us, E4M3 84 ->
+      // 80 us on the capacity combine)
+      if (FMT == kFmtBf16 && nk <= 2)
         combine_token<FMT, 2, LOADS / 2>(nk, cbeg, cend, lane, p, wv, sv, yrow);
       else if (nk <= 4)
         combine_token<FMT, 4, LOADS / 4>(nk, cbeg, cend, lane, p, wv, sv, yrow);

@@ -55,6 +55,14 @@ constexpr long long kCopyPolls = 1ll << 22;
 // of the work.
 constexpr int kOwnPerGroup = 8;
 constexpr int kOwnPerWarp = 4;
+
+// Warps per token in the coded scatter (each thread codes 32 elements) and
+// token groups per CTA.
+__host__ __device__ constexpr int coded_group_warps(int H) { return ((((H >> 4) + 1) >> 1) + 31) >> 5; }
+__host__ __device__ constexpr int coded_groups(int H) {
+  return (kFusedBlock / 32) / coded_group_warps(H) < kFusedMaxGroups ? (kFusedBlock / 32) / coded_group_warps(H)
+                                                                      : kFusedMaxGroups;
+}
 // x rows are preloaded into shared memory only when a whole tile's rows fit in
 // kPreloadBytes (small batches: each CTA then scatters exactly its own tile,
 // with no wait on any other CTA). Otherwise nothing is preloaded: the SM's
@@ -316,6 +324,15 @@ __global__ void __launch_bounds__(kFusedBlock, 1) route_dispatch_fused_kernel(co
   const int64_t row_bytes = 2 * static_cast<int64_t>(a.H);
   FusedSmem s = carve_fused(smem_raw, a.E, a.TW, P, a.H);
 
+  // tokens of the scatter's own part (TokenPlan): the whole tile in own-tile mode
+  int own = a.tile;
+  if (!own_tile) {
+    if constexpr (FMT == kFmtBf16)
+      own = min(a.tile, kOwnPerWarp * (kFusedBlock / 32));
+    else
+      own = min(a.tile, kOwnPerGroup * coded_groups(a.H));
+  }
+
   if (tid == 0) mbar_init(&xbar, 1);
   for (int i = tid; i < a.E * a.TW; i += kFusedBlock) s.mask[i] = 0u;
   pdl_wait();  // logits and x may come from the kernel before this one
@@ -442,7 +459,6 @@ __global__ void __launch_bounds__(kFusedBlock, 1) route_dispatch_fused_kernel(co
     const int end = a.T;
     // the token sequence of this warp (lane 0): its share of the own part,
     // then the shared part (own-tile mode: the whole tile is the own part)
-    const int own = own_tile ? a.tile : min(a.tile, kOwnPerWarp * (kFusedBlock / 32));
     const TokenPlan tp{a.work, a.bar.round, a.status, round, a.T, a.tile, own, static_cast<int>(t0),
                        static_cast<int>(t0) + min(nt, own)};
     int own_next = static_cast<int>(t0) + warp;
@@ -512,8 +528,8 @@ __global__ void __launch_bounds__(kFusedBlock, 1) route_dispatch_fused_kernel(co
     // next. The next token's row is loaded while this one is coded, and the
     // rows two tokens ahead, so that no exchange waits for a load.
     const int ngrp16 = a.H >> 4;
-    const int gw = (((ngrp16 + 1) >> 1) + 31) >> 5;  // warps per token
-    const int ngroups = min((kFusedBlock / 32) / gw, kFusedMaxGroups);
+    const int gw = coded_group_warps(a.H);  // warps per token
+    const int ngroups = coded_groups(a.H);
     const int g = warp / gw;
     if (g < ngroups) {
       const int gsz = gw * 32;
@@ -528,7 +544,6 @@ __global__ void __launch_bounds__(kFusedBlock, 1) route_dispatch_fused_kernel(co
       const int end = a.T;
       // the group's token sequence (thread 0): its share of the own part,
       // then the shared part (own-tile mode: the whole tile is the own part)
-      const int own = own_tile ? a.tile : min(a.tile, kOwnPerGroup * ngroups);
       const TokenPlan tp{a.work, a.bar.round, a.status, round, a.T, a.tile, own, static_cast<int>(t0),
                          static_cast<int>(t0) + min(nt, own)};
       int own_next = static_cast<int>(t0) + g;
