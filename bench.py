@@ -811,6 +811,69 @@ def run_bitmap(args):
     return 0
 
 
+def run_combine_only(args):
+    """ep_combine alone on the workload's layout, for each expert-output
+    format asked for (bf16 rows, or int8 / E4M3 / int4 codes with per-row
+    scales made by ep_quantize_rows*): each one CUDA graph of K launches.
+    Bytes per launch: N*H*b_out (+ N*4 scales) read, T*H*2 written."""
+    import torch
+
+    from combine_warp_top_fp32_b300 import binding as ep
+    from combine_warp_top_fp32_b300 import workloads
+
+    torch.cuda.set_device(0)
+    w = workloads.WORKLOADS[args.workload]
+    cfg = ep.config_from_workload(w, payload=PAYLOAD_MODE[args.payload])
+    d = workloads.generate(w, device="cuda")
+    buf = ep.EpBuffers.allocate(cfg)
+    buf.route_dispatch(d["logits"], d["x"])
+    torch.cuda.synchronize()
+    n_rows = int(buf.expert_off[-1].item())
+    eo = d["expert_out"]
+    rows, H = eo.shape
+    peak, peak_src = measured_peak_gbs()
+
+    def coded(fmt):
+        if fmt == "bf16":
+            return eo, None
+        q = torch.empty((rows, H // 2 if fmt == "int4" else H), dtype=torch.int8 if fmt == "int8" else torch.uint8,
+                        device="cuda")
+        sc = torch.empty(rows, dtype=torch.float32, device="cuda")
+        {"int8": ep.ep_quantize_rows, "fp8": ep.ep_quantize_rows_fp8, "int4": ep.ep_quantize_rows_int4}[fmt](eo, q, sc)
+        return q, sc
+
+    out = {}
+    for fmt in args.combine_only.split(","):
+        o, sc = coded(fmt)
+        for _ in range(args.warmup):
+            buf.combine(o, sc)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            for _ in range(args.steps):
+                buf.combine(o, sc)
+        g.replay()
+        best = float("inf")
+        for _ in range(3):
+            t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            t0.record()
+            g.replay()
+            t1.record()
+            torch.cuda.synchronize()
+            best = min(best, 1e3 * t0.elapsed_time(t1) / args.steps)
+        if ep.ep_get_error(buf.ws) != ep.EP_OK:
+            raise RuntimeError("ep_combine reported a device error")
+        nbytes = int(n_rows * H * PAYLOAD_BYTES[fmt]) + (n_rows * 4 if fmt != "bf16" else 0) + w.T * H * 2
+        out[fmt] = {"us": best, "bytes": nbytes, "gbs": nbytes / best / 1e3, "frac_of_" + peak_src: nbytes / best / 1e3 / peak,
+                    "elements_per_s": n_rows * H / (best * 1e-6)}
+    first = next(iter(out.values()))
+    line = {"metric": "ep_combine alone, by expert-output format", "value": first["us"], "unit": "us per launch",
+            "higher_is_better": False, "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "data": "synthetic",
+            "config": workload_config(w, args.payload, n_rows, False, "fused"), "combine": out}
+    print(json.dumps(line))
+    return 0
+
+
 def parse_args(argv=None):
     ap = argparse.ArgumentParser(description="MoE dispatch+combine benchmark")
     ap.add_argument("--gpus", type=int, default=1)
@@ -823,6 +886,8 @@ def parse_args(argv=None):
                     help="fused: ep_route_dispatch + ep_combine; calls: ep_route, ep_dispatch, ep_combine")
     ap.add_argument("--pipeline", default=None,
                     help="comma-separated chunk counts: time the chunked pipeline with stand-in GEMM experts")
+    ap.add_argument("--combine-only", default=None, metavar="FMTS",
+                    help="comma-separated expert-output formats (bf16,int8,fp8,int4): time ep_combine alone")
     ap.add_argument("--bitmap", action="store_true",
                     help="report the bitmap routing metadata (bytes saved, encode and layout times)")
     ap.add_argument("--no-e2e", action="store_true")
@@ -856,6 +921,8 @@ def main(argv=None):
         return run_pipeline(args)
     if args.bitmap:
         return run_bitmap(args)
+    if args.combine_only:
+        return run_combine_only(args)
     return run_gpu(args)
 
 

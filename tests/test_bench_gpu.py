@@ -57,3 +57,33 @@ def test_bench_line_on_decode_latency(monkeypatch):
     both = d["int8_both_directions"]
     assert both["value"] > 0 and both["bytes_per_step"] < d["hbm"]["bytes_per_step"]
     assert {"sm_mhz", "sm_max_mhz", "reasons"} <= set(d["clocks"])
+
+
+def test_combine_only_line(monkeypatch):
+    """bench.py --combine-only: one line with every format asked for, its
+    bytes per launch as the docstring counts them, and a positive time."""
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA GPU")
+    import bench
+    from combine_warp_top_fp32_b300 import workloads
+
+    monkeypatch.delenv("RANK", raising=False)
+    monkeypatch.delenv("WORLD_SIZE", raising=False)
+    buf = io.StringIO()
+    with redirect_stdout(buf):
+        rc = bench.main(["--workload", "prefill-mid", "--combine-only", "bf16,int8,fp8,int4", "--steps", "3",
+                         "--warmup", "3"])
+    assert rc == 0
+    lines = [ln for ln in buf.getvalue().splitlines() if ln.startswith("{")]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    w = workloads.WORKLOADS["prefill-mid"]
+    n = d["config"]["rows_dispatched"]
+    assert n == w.T * w.k  # dropless
+    per = {"bf16": 2, "int8": 1, "fp8": 1, "int4": 0.5}
+    assert list(d["combine"]) == ["bf16", "int8", "fp8", "int4"]
+    for fmt, rec in d["combine"].items():
+        assert rec["us"] > 0
+        assert rec["bytes"] == int(n * w.H * per[fmt]) + (n * 4 if fmt != "bf16" else 0) + w.T * w.H * 2
+        assert rec["gbs"] == pytest.approx(rec["bytes"] / rec["us"] / 1e3)
+    assert d["value"] == d["combine"]["bf16"]["us"]

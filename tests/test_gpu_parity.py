@@ -286,17 +286,26 @@ def test_empty_batch(ep):
 
 
 @pytest.mark.parametrize("fmt", ["int8", "fp8", "int4"])
-@pytest.mark.parametrize("shape", ["prefill-mid", "wide"])
+@pytest.mark.parametrize("shape", ["prefill-mid", "wide", "many-slots", "many-slots-drops", "short"])
 def test_coded_return_path(ep, orc, shape, fmt):
-    """Expert outputs coded per row (ep_quantize_rows / ep_quantize_rows_fp8)
-    then combined from the codes (prefill-mid: 2 KB rows; wide: 8 KB rows,
-    with drops)."""
+    """Expert outputs coded per row (ep_quantize_rows / _fp8 / _int4) then
+    combined from the codes. prefill-mid: 2 KB rows; wide: 8 KB rows, with
+    drops; many-slots: k = 16, every slot kept (more than 8 kept slots: the
+    sum runs in groups of 8 with the accumulators carried); many-slots-drops:
+    k = 12 with heavy drops (0 to 12 kept slots per token); short: T = 37, so
+    each token's row is cut into slices."""
     from combine_warp_top_fp32_b300 import workloads
 
     fp8, int4 = fmt == "fp8", fmt == "int4"
     w = workloads.WORKLOADS["prefill-mid"]
     if shape == "wide":
         w = w.replace(T=1500, H=8192, capacity_factor=1.0, seed=9)
+    elif shape == "many-slots":
+        w = w.replace(T=700, H=1024, E=64, k=16, capacity_factor=0.0, seed=11)
+    elif shape == "many-slots-drops":
+        w = w.replace(T=900, H=2048, E=32, k=12, capacity_factor=0.5, seed=12)
+    elif shape == "short":
+        w = w.replace(T=37, H=4096, E=64, k=6, capacity_factor=0.0, seed=13)
     kind = {"int8": ep.EP_PAYLOAD_INT8, "fp8": ep.EP_PAYLOAD_FP8, "int4": ep.EP_PAYLOAD_INT4}[fmt]
     cfg = ep.config_from_workload(w, payload=kind)
     d = workloads.generate(w, device="cuda")
