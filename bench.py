@@ -869,7 +869,9 @@ def run_combine_only(args):
     first = next(iter(out.values()))
     line = {"metric": "ep_combine alone, by expert-output format", "value": first["us"], "unit": "us per launch",
             "higher_is_better": False, "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "data": "synthetic",
-            "config": workload_config(w, args.payload, n_rows, False, "fused"), "combine": out}
+            "config": dict(workload_config(w, args.payload, n_rows, False, "fused"), expert_out=args.combine_only,
+                           path="ep_combine alone (layout from ep_route_dispatch)"),
+            "combine": out}
     print(json.dumps(line))
     return 0
 
