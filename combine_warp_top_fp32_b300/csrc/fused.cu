@@ -102,11 +102,12 @@ struct FusedSmem {
   uint32_t* pre;        // [E][TW] set bits of e in the words before w
   int* base;            // [E] pairs of e in earlier tiles
   int* kept;            // [E] kept pairs of e (then the expert offsets)
-  int* drop;            // [E]
+  uint8_t* ids;         // [32 TW][k] the expert of each pair of the tile (E <= 256), from the routing
 };
 
-__host__ __device__ inline size_t fused_smem_fixed(int E, int TW) {
-  return static_cast<size_t>(E) * TW * 8 + static_cast<size_t>(E) * 12 + 64;
+__host__ __device__ inline size_t fused_smem_fixed(int E, int TW, int k) {
+  return static_cast<size_t>(E) * TW * 8 + static_cast<size_t>(E) * 8 + ((static_cast<size_t>(32) * TW * k + 15) & ~15ull) +
+         64;
 }
 
 __device__ __forceinline__ FusedSmem carve_fused(unsigned char* smem, int E, int TW, int npre, int H) {
@@ -117,7 +118,7 @@ __device__ __forceinline__ FusedSmem carve_fused(unsigned char* smem, int E, int
   s.pre = s.mask + E * TW;
   s.base = reinterpret_cast<int*>(s.pre + E * TW);
   s.kept = s.base + E;
-  s.drop = s.kept + E;
+  s.ids = reinterpret_cast<uint8_t*>(s.kept + E);
   return s;
 }
 
@@ -130,7 +131,7 @@ __device__ __forceinline__ void group_sync(int id, int nthreads) {
 // e, placed at e's offset; -1 past the capacity. Writes slot_row / row_slot.
 __device__ __forceinline__ int fused_row(const FusedArgs& a, const FusedSmem& s, int64_t t, int tl, int j) {
   const int64_t p = t * a.k + j;
-  const int e = a.topk_idx[p];  // written by this CTA before a CTA barrier
+  const int e = s.ids[tl * a.k + j];  // the routed expert, kept in shared memory by this CTA
   const int w = tl >> 5;
   const int r = static_cast<int>(s.pre[e * a.TW + w]) + __popc(s.mask[e * a.TW + w] & ((1u << (tl & 31)) - 1u));
   const int pos = s.base[e] + r;
@@ -314,6 +315,7 @@ __global__ void __launch_bounds__(kFusedBlock, 1) route_dispatch_fused_kernel(co
   __shared__ int32_t rows_s[kFusedMaxGroups][3][32];  // per token group: its next tokens' rows (three deep)
   __shared__ float amax_s[kFusedMaxGroups][2][16];    // per token group: its warps' amax
   __shared__ int ids_s[kFusedMaxGroups][2];           // per token group: the token after next
+  __shared__ int scan_s[16];                          // the offsets' warp sums and drops
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int b = blockIdx.x, G = gridDim.x;
   const int64_t t0 = static_cast<int64_t>(b) * a.tile;
@@ -353,7 +355,8 @@ __global__ void __launch_bounds__(kFusedBlock, 1) route_dispatch_fused_kernel(co
   };
 
   // ---- A: route the tile and count it ---------------------------------------
-  route_tile<VPL, VEC4>(a.logits, t0, nt, a.E, a.k, a.lanes_log2, a.renorm, a.TW, s.mask, a.topk_idx, a.topk_w);
+  route_tile<VPL, VEC4>(a.logits, t0, nt, a.E, a.k, a.lanes_log2, a.renorm, a.TW, s.mask, a.topk_idx, a.topk_w,
+                        s.ids);
   __syncthreads();
   tile_word_prefix_row(s.mask, s.pre, a.E, a.TW, a.counts + static_cast<int64_t>(b) * a.E);
 
@@ -380,42 +383,45 @@ __global__ void __launch_bounds__(kFusedBlock, 1) route_dispatch_fused_kernel(co
       tile_bases(a.counts, G, a.E, b, s.base, s.kept);
     }
     __syncthreads();
-    if (warp == 0) {  // capacity clip and the expert offsets: one warp, 8 experts per lane (E <= 256)
-      constexpr int PL = kFusedMaxExperts / 32;
-      const int e0 = lane * PL;
-      int kept[PL], kept_run = 0, drop_run = 0;
-#pragma unroll
-      for (int i = 0; i < PL; ++i) {
-        const int e = e0 + i;
-        const int raw = e < a.E ? s.kept[e] : 0;
-        kept[i] = min(raw, a.cap);
-        kept_run += kept[i];
-        drop_run += raw - kept[i];
-        if (b == 0 && e < a.E) {
-          a.expert_counts[e] = kept[i];
-          if (a.expert_raw) a.expert_raw[e] = raw;
+    // capacity clip and the expert offsets: thread e < E of the first 8 warps
+    // holds expert e (E <= 256); warp sums meet in shared memory
+    {
+      const bool on = tid < a.E;
+      int raw = 0, kept = 0, incl = 0;
+      if (warp < 8) {
+        raw = on ? s.kept[tid] : 0;
+        kept = min(raw, a.cap);
+        incl = warp_inclusive_scan(kept);
+        const unsigned drop = __reduce_add_sync(0xffffffffu, static_cast<unsigned>(raw - kept));
+        if (lane == 31) {
+          scan_s[warp] = incl;
+          scan_s[8 + warp] = static_cast<int>(drop);
         }
       }
-      const int kept_incl = warp_inclusive_scan(kept_run);
-      const int drop_tot = __reduce_add_sync(0xffffffffu, static_cast<unsigned>(drop_run));
-      int off = kept_incl - kept_run;
-      const int Gr = a.E / a.R;  // rank r starts at its first expert r*Gr
+      __syncthreads();
+      if (on) {  // tid < E <= 256: warps 0..7
+        int before = 0, total = 0, drop_tot = 0;
 #pragma unroll
-      for (int i = 0; i < PL; ++i) {
-        const int e = e0 + i;
-        if (e < a.E) {
-          s.kept[e] = off;  // from here on: the expert's offset
-          if (b == 0) {
-            a.expert_off[e] = off;
-            if (e % Gr == 0) a.rank_off[e / Gr] = off;
+        for (int w = 0; w < 8; ++w) {
+          const int v = scan_s[w];
+          total += v;
+          if (w < warp) before += v;
+          drop_tot += scan_s[8 + w];
+        }
+        const int off = before + incl - kept;
+        s.kept[tid] = off;  // from here on: the expert's offset
+        if (b == 0) {
+          const int Gr = a.E / a.R;  // rank r starts at its first expert r*Gr
+          a.expert_counts[tid] = kept;
+          if (a.expert_raw) a.expert_raw[tid] = raw;
+          a.expert_off[tid] = off;
+          if (tid % Gr == 0) a.rank_off[tid / Gr] = off;
+          if (tid == a.E - 1) {
+            a.expert_off[a.E] = total;
+            a.rank_off[a.R] = total;
+            *a.n_dropped = drop_tot;
           }
         }
-        off += kept[i];
-      }
-      if (b == 0 && lane == 31) {
-        a.expert_off[a.E] = kept_incl;
-        a.rank_off[a.R] = kept_incl;
-        *a.n_dropped = drop_tot;
       }
     }
     __syncthreads();
@@ -710,7 +716,7 @@ cudaError_t launch_fused_t(FusedArgs fa, int G, cudaStream_t s, bool dry) {
   auto kernel = route_dispatch_fused_kernel<VPL, VEC4, FMT>;
   static int prep[64], carve[64], static_smem[64];
   const int dyn = fused_prepare(kernel, prep);
-  const size_t fixed = fused_smem_fixed(fa.E, fa.TW);
+  const size_t fixed = fused_smem_fixed(fa.E, fa.TW, fa.k);
   if (dyn < 0 || static_cast<size_t>(dyn) < fixed) return cudaErrorNotSupported;
   if (dry) return cudaSuccess;
   // the static tail: as many x rows per CTA as shared memory holds, at most

@@ -495,12 +495,15 @@ __device__ __forceinline__ void route_warp(const float* __restrict__ logits, int
 // per token; with L = 32, two tokens per warp in flight up to 4 values per
 // lane and one above, the next ones' logits loaded meanwhile), writes their
 // slots and sets their bits in the tile's per-expert masks in shared memory:
-// mask[e][w] bit b = token 32w+b of the tile chose e. The masks must be zero
-// on entry; the caller synchronises the CTA afterwards.
+// mask[e][w] bit b = token 32w+b of the tile chose e, and, when `ids` is
+// given (E <= 256), ids[tl * k + j] = the expert of the tile's token tl in
+// slot j. The masks must be zero on entry; the caller synchronises the CTA
+// afterwards.
 template <int VPL, bool VEC4>
 __device__ __forceinline__ void route_tile(const float* __restrict__ logits, int64_t t0, int nt, int E, int k,
                                            int lanes_log2, int renorm, int TW, uint32_t* mask,
-                                           int32_t* __restrict__ topk_idx, float* __restrict__ topk_w) {
+                                           int32_t* __restrict__ topk_idx, float* __restrict__ topk_w,
+                                           uint8_t* ids = nullptr) {
   const int L = 1 << lanes_log2;
   const int lane = threadIdx.x & 31;
   const int warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
@@ -508,6 +511,7 @@ __device__ __forceinline__ void route_tile(const float* __restrict__ logits, int
     topk_idx[t * k + lane] = e;
     topk_w[t * k + lane] = w;
     atomicOr(&mask[e * TW + static_cast<int>(tl >> 5)], 1u << (tl & 31));
+    if (ids) ids[tl * k + lane] = static_cast<uint8_t>(e);
   };
   if constexpr (VPL <= 8) {
     if (L == 32) {
@@ -530,6 +534,7 @@ __device__ __forceinline__ void route_tile(const float* __restrict__ logits, int
       topk_idx[t * k + sub] = e;
       topk_w[t * k + sub] = w;
       atomicOr(&mask[e * TW + (tl >> 5)], 1u << (tl & 31));
+      if (ids) ids[tl * k + sub] = static_cast<uint8_t>(e);
     }
   }
 }
