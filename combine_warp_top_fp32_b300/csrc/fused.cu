@@ -1,4 +1,4 @@
-// fused.cu — ep_route_dispatch in one persistent launch: route, lay out and
+// fused.cu — ep_route_dispatch in one cooperative launch: route, lay out and
 // scatter a batch with one CTA per SM.
 //
 // The ThunderEP article (bjdmk.com.cn, §5.2) suggests fusing the bucketing by
@@ -21,14 +21,20 @@
 //      article, hotelren.com, §3.3: running sums of the send counts); CTA 0
 //      writes the layout outputs; each CTA writes its own pairs' rows
 //      (slot_row / row_slot).
-//   -- grid barrier 2 (not for small batches): every pair's row is written --
+//   -- grid barrier 2, split: each CTA arrives when its pairs' rows are
+//      written and waits only before it takes another tile's tokens --
 //   C  scatter the payload: bf16 copies (a warp per token) or the per-token
 //      int8 / FP8 / int4 code (ThunderEP §2.3; a group of warps per token with
-//      its own named barrier). Small batches: each CTA its own tile, x from
-//      shared memory. Otherwise every group of every CTA takes the batch's
-//      tokens in order from one shared counter, so that the SMs, which move
-//      data at different speeds, and the tokens, whose kept rows differ
-//      (capacity drops fall on the later ones), even out.
+//      its own named barrier). First the first tokens of the CTA's own tile,
+//      then (after barrier 2) the rest of every tile from one shared counter,
+//      so that the SMs, which move data at different speeds, and the tokens,
+//      whose kept rows differ (capacity drops fall on the later ones), even
+//      out. Small batches: each CTA its own tile, x from shared memory, and
+//      nothing shared.
+//
+// Both barriers count arrivals on one word (count_barrier, split_arrive): the
+// first completes at G arrivals, the second at 2G, whose last arrival zeroes
+// the words for the next launch.
 //
 // Every output equals that of route_count_kernel + scan_kernel + the scatter
 // kernels, bit for bit (the same routing, the same row rule, the same codes).
@@ -90,7 +96,7 @@ struct FusedArgs {
   int32_t* counts;  // workspace: [G][E] per-tile counts
   uint32_t* status;
   GridBarrier bar;
-  unsigned* work;  // the scatter's shared token counter, zeroed at the first grid barrier
+  unsigned* work;  // the scatter's shared token counter, zeroed by the second barrier's last arrival
   int extra_arrivals;  // > 0 only when a test forces the barrier to time out
   long long barrier_polls;
 };
@@ -270,7 +276,7 @@ __device__ __forceinline__ void tile_bases(const int32_t* __restrict__ counts, i
 // (resolve), so no group waits on the atomic. One thread per group calls
 // these.
 struct TokenPlan {
-  unsigned* work;           // the shared counter (zeroed at the first grid barrier)
+  unsigned* work;           // the shared counter (zeroed when the second barrier completes)
   const unsigned* round;    // the grid barrier's round word
   uint32_t* status;
   unsigned round_before;    // the round while the second barrier is incomplete
@@ -361,7 +367,8 @@ __global__ void __launch_bounds__(kFusedBlock, 1) route_dispatch_fused_kernel(co
   tile_word_prefix_row(s.mask, s.pre, a.E, a.TW, a.counts + static_cast<int64_t>(b) * a.E);
 
   unsigned round = 0u;
-  bool ok = grid_barrier(a.bar, static_cast<unsigned>(G + a.extra_arrivals), a.barrier_polls, a.work, 0u, &round);
+  const unsigned expected = static_cast<unsigned>(G + a.extra_arrivals);
+  bool ok = count_barrier(a.bar, expected, a.barrier_polls, &round);
 
   if (ok) {
     // ---- B: this tile's first position within each expert, the offsets ------
@@ -433,7 +440,7 @@ __global__ void __launch_bounds__(kFusedBlock, 1) route_dispatch_fused_kernel(co
     // this tile's rows are written: arrive at the second grid barrier (its
     // wait comes when the own part is done)
     __syncthreads();
-    if (tid == 0 && !own_tile) grid_arrive(a.bar, static_cast<unsigned>(G + a.extra_arrivals));
+    if (tid == 0) split_arrive(a.bar, expected, a.work);  // in own-tile mode too: the last arrival resets the words
   }
   if (!ok) {
     if (tid == 0) {

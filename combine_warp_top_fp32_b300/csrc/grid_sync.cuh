@@ -1,4 +1,4 @@
-// grid_sync.cuh — the one device-wide wait of the fused dispatch kernel, and
+// grid_sync.cuh — the device-wide waits of the fused dispatch kernel, and
 // the bounded waits on its bulk copies.
 //
 // The fused kernel is launched cooperatively (every CTA resident at once), so
@@ -13,10 +13,9 @@
 
 namespace ep {
 
-// Barrier words in the workspace: arrivals of the current round and the
-// round number. The last CTA to arrive zeroes the arrivals and then advances
-// the round; the others wait for the round to change. Arrivals are back at 0
-// after every completed barrier, so a workspace zeroed once serves every call.
+// Barrier words in the workspace: an arrival count and a round number
+// (count_barrier / split_arrive below). Both are back at their resting state
+// after every completed launch, so a workspace zeroed once serves every call.
 struct GridBarrier {
   unsigned* count;
   unsigned* round;
@@ -38,33 +37,28 @@ __device__ __forceinline__ void red_add_release_gpu(unsigned* p, unsigned v) {
   asm volatile("red.add.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 
-// All threads of the CTA call it. Returns true once every one of `expected`
-// CTAs has arrived (their writes before the barrier are then visible to every
-// thread of this CTA), false if thread 0 gave up after `limit` polls. The
-// CTA's writes reach thread 0 through the CTA barrier; thread 0's arrival is
-// a release and its wait an acquire at GPU scope. The last CTA to arrive
-// also stores `reset_value` to `*reset` (when given) before it lets the others
-// go, so a counter used after the barrier starts from a known value.
-// *round_after (when given) receives the round the barrier completes: the
-// same in every CTA, and different in consecutive uses of the words.
-__device__ __forceinline__ bool grid_barrier(GridBarrier bar, unsigned expected, long long limit,
-                                             unsigned* reset = nullptr, unsigned reset_value = 0u,
-                                             unsigned* round_after = nullptr) {
+// The single launch's two grid-wide waits on one arrival count. The first
+// completes when the count reaches `expected` (every CTA arrived once): no
+// CTA resets anything, so the waiters see completion one L2 round trip after
+// the last arrival. The second (split_arrive, below) counts on to
+// 2 * expected; its last arrival zeroes the count and `reset` (the scatter's
+// token counter) and advances the round, which the second wait polls. The
+// words are back at zero after every launch. All threads of the CTA call
+// count_barrier; it returns false if thread 0 gave up after `limit` polls.
+// *round_out (thread 0's read, shared with the CTA) is the round while the
+// second wait is incomplete.
+__device__ __forceinline__ bool count_barrier(GridBarrier bar, unsigned expected, long long limit,
+                                              unsigned* round_out) {
   __shared__ int passed_s;
   __shared__ unsigned round_s;
   __syncthreads();
   if (threadIdx.x == 0) {
     int passed = 1;
-    const unsigned r = ld_acquire_gpu(bar.round);
-    round_s = r + 1u;
     const unsigned prev = atom_add_acq_rel_gpu(bar.count, 1u);
-    if (prev == expected - 1) {
-      *reinterpret_cast<volatile unsigned*>(bar.count) = 0u;
-      if (reset) *reinterpret_cast<volatile unsigned*>(reset) = reset_value;
-      red_add_release_gpu(bar.round, 1u);
-    } else {
+    round_s = ld_acquire_gpu(bar.round);  // unchanged until the second wait completes
+    if (prev + 1u < expected) {
       long long polls = 0;
-      while (ld_acquire_gpu(bar.round) == r) {
+      while (ld_acquire_gpu(bar.count) < expected) {
         if (++polls > limit) {
           passed = 0;
           break;
@@ -75,19 +69,17 @@ __device__ __forceinline__ bool grid_barrier(GridBarrier bar, unsigned expected,
     passed_s = passed;
   }
   __syncthreads();
-  if (round_after) *round_after = round_s;
+  *round_out = round_s;
   return passed_s != 0;
 }
 
-// The arrival half of a split grid barrier, by one thread after a CTA
-// barrier (so the CTA's writes before it are ordered before the arrival): the
-// last of `expected` CTAs to arrive zeroes the arrivals and advances the round.
-// The wait half is a bounded poll until the round differs from the one seen at
-// the barrier before (every CTA knows it).
-__device__ __forceinline__ void grid_arrive(GridBarrier bar, unsigned expected) {
+// The second wait's arrival (one thread, after a CTA barrier): the last of
+// 2 * expected arrivals zeroes the count and *reset, then advances the round.
+__device__ __forceinline__ void split_arrive(GridBarrier bar, unsigned expected, unsigned* reset) {
   const unsigned prev = atom_add_acq_rel_gpu(bar.count, 1u);
-  if (prev == expected - 1) {
+  if (prev == 2u * expected - 1u) {
     *reinterpret_cast<volatile unsigned*>(bar.count) = 0u;
+    *reinterpret_cast<volatile unsigned*>(reset) = 0u;
     red_add_release_gpu(bar.round, 1u);
   }
 }
