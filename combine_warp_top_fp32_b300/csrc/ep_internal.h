@@ -49,7 +49,7 @@ inline WsLayout ws_layout(int T, int E, int k) {
   const size_t count_slots = static_cast<size_t>(E) *
                              static_cast<size_t>(L.ntiles > fused_ctas ? L.ntiles : fused_ctas) * sizeof(int32_t);
   L.status_off = 0;
-  L.ticket_off = 4;
+  L.ticket_off = 4;  // the combine's unit counter and its warps-done count at 64 and 68
   L.bar_off = 128;  // the grid barrier's arrivals at 128, its round at 256 and the fused scatter's token
                     // counter at 384, each on a 128-byte line of its own (the round is polled while the
                     // arrivals are counted, the counter taken from all the while)
@@ -256,6 +256,7 @@ struct CombineArgs {
   const float* topk_w;
   void* y;
   uint32_t* status;
+  unsigned* counter;  // two words of the workspace (zero between calls): a unit counter and the warps done; or null
 };
 
 cudaError_t launch_combine(const CombineArgs& a, int sms, cudaStream_t s);

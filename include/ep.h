@@ -24,7 +24,10 @@
  *   - All array pointers are caller-owned device memory unless stated; the
  *     library allocates nothing and keeps no state between calls apart from
  *     per-device launch settings. Scratch comes from a caller-provided
- *     workspace sized by ep_workspace_size().
+ *     workspace sized by ep_workspace_size(). Its counters and wait words
+ *     are back at zero when each call completes; calls that share a
+ *     workspace must not run at the same time on the GPU (issue them on one
+ *     stream, or order them with events).
  *   - Calls are asynchronous on the given stream (0 = legacy default stream)
  *     and never synchronise it, except ep_get_error().
  *   - Errors are returned, never raised by exit/abort (the NCCL EP article,
@@ -297,7 +300,9 @@ ep_status_t ep_dispatch_static(const ep_config_t* cfg, const void* x, const int3
  *                                  v_j = float(bf16) or (float)q * scale
  *                                  (q the int8, E4M3 or int4 code, widened
  *                                  exactly)
- *   ws, ws_bytes workspace (its status word records bad slot_row entries)
+ *   ws, ws_bytes workspace, at least 256 bytes (its status word records bad
+ *                slot_row entries; two words at byte 64 count the units of
+ *                work that the warps take, and are zero again on return)
  * A token whose k slots were all dropped gets y = 0. The E4M3 NaN codes (0x7F,
  * 0xFF), which no encoder of this library writes, are outside the contract
  * (they read as +-480).
