@@ -25,9 +25,9 @@
  *     library allocates nothing and keeps no state between calls apart from
  *     per-device launch settings. Scratch comes from a caller-provided
  *     workspace sized by ep_workspace_size(). Its counters and wait words
- *     are back at zero when each call completes; calls that share a
- *     workspace must not run at the same time on the GPU (issue them on one
- *     stream, or order them with events).
+ *     need no reset between calls (each call leaves them as the next one
+ *     expects); calls that share a workspace must not run at the same time
+ *     on the GPU (issue them on one stream, or order them with events).
  *   - Calls are asynchronous on the given stream (0 = legacy default stream)
  *     and never synchronise it, except ep_get_error().
  *   - Errors are returned, never raised by exit/abort (the NCCL EP article,

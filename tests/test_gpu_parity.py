@@ -429,6 +429,35 @@ def test_deterministic_bytes(ep):
         assert torch.equal(a, b)
 
 
+def test_wait_and_work_words_return_to_zero(ep):
+    """Every call leaves the workspace's words where the next call expects
+    them: after capacity steps the single launch's arrival count and the bf16
+    combine's unit counter and warps-done count (used at this shape) are back
+    at zero (the scatter's token counter is zeroed by the second barrier,
+    before any CTA takes from it, so its end value does not matter), and five
+    repeated steps give the same bytes as the first."""
+    from combine_warp_top_fp32_b300 import workloads
+
+    w = workloads.WORKLOADS["capacity"]
+    cfg = ep.config_from_workload(w, payload=ep.EP_PAYLOAD_INT8)
+    d = workloads.generate(w, device="cuda")
+    buf = ep.EpBuffers.allocate(cfg)
+    buf.route_dispatch(d["logits"], d["x"])
+    buf.combine(d["expert_out"])
+    torch.cuda.synchronize()
+    first = [t.clone() for t in (buf.payload, buf.slot_row, buf.y)]
+    for _ in range(5):
+        buf.route_dispatch(d["logits"], d["x"])
+        buf.combine(d["expert_out"])
+    torch.cuda.synchronize()
+    assert ep.ep_get_error(buf.ws) == ep.EP_OK
+    words = buf.ws[:512].view(torch.int32).cpu().numpy()
+    assert words[64 // 4] == 0 and words[68 // 4] == 0  # the combine's unit counter, warps done
+    assert words[128 // 4] == 0  # the grid barrier's arrival count
+    for a, b in zip(first, (buf.payload, buf.slot_row, buf.y)):
+        assert torch.equal(a, b)
+
+
 # ----------------------------------------------------------------------------
 # device-side index checks: bad inputs become a status code, never an access
 # ----------------------------------------------------------------------------
