@@ -73,17 +73,12 @@ ep_status_t from_cuda(cudaError_t e) { return e == cudaSuccess ? EP_OK : EP_ERR_
 
 int g_route_dispatch_form = EP_FORM_AUTO;  // ep_debug_set(EP_DEBUG_ROUTE_DISPATCH_FORM, ...)
 
-// Whether ep_route_dispatch's single cooperative launch beats the kernel
-// chain, by batch shape (measured on the B300): it does for large batches,
-// where every SM takes tokens from one counter and the scan kernel and its
-// boundary go away, and for small ones with E >= 32, where the layout comes
-// from the routed ids; in between (a few thousand tokens) its fixed cost (two
-// device-wide waits, every CTA reading every tile's counts) is more than the
-// chain's, and with E < 32 the cluster form of the chain is quicker.
-bool single_launch_pays(const ep_config_t* c) {
-  if (c->T >= 8192) return true;
-  return static_cast<int64_t>(c->T) * c->k <= 8192 && c->E >= 32;
-}
+// Whether the single launch beats the chain by default (measured on the
+// B300): with E >= 32 at every batch size measured (128 to 131,072 tokens;
+// e.g. 4,096 tokens, E = 64: 49-50 against 56 us a step with bf16
+// payloads), and with large batches (T >= 8192) at any E; with E < 32 on
+// small batches the cluster form of the chain is quicker.
+bool single_launch_pays(const ep_config_t* c) { return c->T >= 8192 || c->E >= 32; }
 
 // The form ep_route_dispatch takes for a call whose arguments passed the
 // checks: the single launch (if chosen and it can run here), the cluster form
