@@ -86,7 +86,7 @@ struct FusedArgs {
   int T, H, E, k, R, cap, renorm, lanes_log2;
   int tile, TW;        // tokens per tile, mask words per expert (a power of two)
   int npre;            // x rows preloaded per CTA (its own tile's), 0 for none
-  int own_tile;        // 1: each CTA scatters its own tile (no second barrier)
+  int own_tile;        // 1: each CTA scatters its whole tile (nothing shared, no wait at the second barrier)
   int small_layout;    // 1: the layout comes from the routed ids, not the tile counts
   int32_t* topk_idx;
   float* topk_w;
@@ -328,7 +328,7 @@ __global__ void __launch_bounds__(kFusedBlock, 1) route_dispatch_fused_kernel(co
   const int nt = static_cast<int>(min(static_cast<int64_t>(a.tile), a.T - t0));  // >= 1: G = ceil(T / tile)
   const int P = min(a.npre, nt);          // preloaded tokens of this CTA's own tile (the last may be short)
   const int tail0 = static_cast<int>(t0);  // the preloaded rows are tokens [t0, t0 + P)
-  const bool own_tile = a.own_tile != 0;  // the CTA scatters its own tile (then no second barrier)
+  const bool own_tile = a.own_tile != 0;  // the CTA scatters its own tile (and never waits at the second barrier)
   const int64_t row_bytes = 2 * static_cast<int64_t>(a.H);
   FusedSmem s = carve_fused(smem_raw, a.E, a.TW, P, a.H);
 
@@ -728,7 +728,7 @@ cudaError_t launch_fused_t(FusedArgs fa, int G, cudaStream_t s, bool dry) {
   if (dry) return cudaSuccess;
   // the static tail: as many x rows per CTA as shared memory holds, at most
   // floor(T / G) so that every CTA has as many; when the tail is each CTA's
-  // own tile, the scatter needs no second grid barrier
+  // own tile, no CTA waits at the second grid barrier
   const int64_t row_bytes = 2 * static_cast<int64_t>(fa.H);
   const int64_t room = static_cast<int64_t>(dyn) - static_cast<int64_t>(fixed);
   const bool small = static_cast<int64_t>(fa.tile) * row_bytes <= (room < kPreloadBytes ? room : kPreloadBytes);

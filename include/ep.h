@@ -184,17 +184,18 @@ ep_status_t ep_dispatch(const ep_config_t* cfg, const void* x, const int32_t* to
  *   ep_dispatch(cfg, x, topk_idx, payload, ..., ws, ws_bytes, stream);
  * would write; the arguments mean what they mean there (logits [T, E] fp32
  * in, 16-byte aligned; topk_idx / topk_w [T, k] out).
- * Single-launch form (large batches, T >= 8192, and small ones, T*k <= 8192
- * with 32 <= E; E <= 256, at most 1024 tokens per SM, x 32-byte aligned,
- * cooperative launch available): one cooperative launch of one CTA per SM
- * does it all. Each CTA routes its own tile of ceil(T / SMs) tokens; one
- * device-wide wait; each CTA forms its tile's positions from every tile's
- * counts (small batches: from all the routed ids) and writes its pairs' rows;
- * then the payload is scattered, each SM taking tokens from a shared counter
- * (a second device-wide wait first), or, for small batches, each CTA its own
- * tile. Those waits are bounded (about a second); if one runs out the call's
- * outputs are not valid and ep_get_error() reports EP_ERR_TIMEOUT (and resets
- * the waits' words in the workspace, so the workspace can be used again).
+ * Single-launch form (by default when 32 <= E <= 256, or T >= 8192 with
+ * E <= 256; at most 1024 tokens per SM, x 32-byte aligned, cooperative
+ * launch available): one cooperative launch of one CTA per SM does it all.
+ * Each CTA routes its own tile of ceil(T / SMs) tokens; one device-wide wait;
+ * each CTA forms its tile's positions from every tile's counts (small
+ * batches: from all the routed ids) and writes its pairs' rows; then it
+ * scatters the first tokens of its own tile and, after a second device-wide
+ * wait, takes the rest of every tile from a shared counter (small batches:
+ * each CTA its whole tile, nothing shared). Those waits are bounded (about a
+ * second); if one runs out the call's outputs are not valid and
+ * ep_get_error() reports EP_ERR_TIMEOUT (and resets the waits' words in the
+ * workspace, so the workspace can be used again).
  * Otherwise three kernels run: a CTA routes one tile of tokens and counts its
  * per-expert copies in shared memory, then the scan and the scatter of
  * ep_dispatch; a batch of at most 256 tokens with E <= 256 then takes two
