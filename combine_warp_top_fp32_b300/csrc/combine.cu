@@ -223,17 +223,20 @@ __global__ void __launch_bounds__(256, combine_min_ctas<FMT>()) combine_kernel(c
   const int ns = a.slices;
   const int cslice = (nchunk + ns - 1) / ns;
   const int64_t units = static_cast<int64_t>(a.T) * ns;
-  // A warp's units: warp0 first, then u + nwarps (static), or, for bf16 rows
-  // with a.counter set (few units a warp: see the launcher), nwarps + the
-  // next value of a shared counter, asked for while the next unit's slots
-  // load; the static order would leave a ragged last round. Each unit's
+  // A warp's units: warp0, warp0 + nwarps, ... (the static order); for bf16
+  // rows with a.counter set (few units a warp: see the launcher) only the
+  // first a.static_rounds of them, then static_end + the next value of a
+  // shared counter, asked for while the next unit's slots load, so that the
+  // warps finish together instead of in a ragged last round. Each unit's
   // slots are loaded one unit ahead.
   unsigned* const ctr = FMT == kFmtBf16 ? a.counter : nullptr;
+  const int64_t static_end = static_cast<int64_t>(a.static_rounds) * nwarps;  // units taken in the static order
   auto claim = [&](int64_t after) -> int64_t {
-    if (!ctr) return after + nwarps;
+    const int64_t next = after + nwarps;
+    if (!ctr || next < static_end) return next;
     unsigned v = 0u;
     if (lane == 0) v = atomicAdd(ctr, 1u);
-    return nwarps + static_cast<int64_t>(__shfl_sync(kFull, v, 0));
+    return static_end + static_cast<int64_t>(__shfl_sync(kFull, v, 0));
   };
   int row_n, row;
   float w_n, sc_n, w, sc;
@@ -350,6 +353,8 @@ namespace {
 
 int g_occ_combine[8][64];
 
+constexpr int64_t kDynamicUnits = 4;  // units per warp taken from the shared counter at the end
+
 template <int FMT, int LOADS>
 cudaError_t launch_combine_t(CombineArgs a, int sms, int* cache, cudaStream_t s) {
   constexpr int kBlock = 256;
@@ -376,6 +381,9 @@ cudaError_t launch_combine_t(CombineArgs a, int sms, int* cache, cudaStream_t s)
   const int64_t per_warp = units / (static_cast<int64_t>(grid) * (kBlock / 32));
   const int64_t unit_bytes = (static_cast<int64_t>(a.k) * a.H * 2 + static_cast<int64_t>(a.H) * 2) / a.slices;
   if (FMT != kFmtBf16 || per_warp < 4 || per_warp >= 32 || unit_bytes < 16 * 1024) a.counter = nullptr;
+  // with the counter, the first units of each warp still follow the static
+  // order (no atomic) and only about the last kDynamicUnits are shared
+  a.static_rounds = static_cast<int>(per_warp > kDynamicUnits ? per_warp - kDynamicUnits : 1);
   return launch_pdl(combine_kernel<FMT, LOADS>, grid, kBlock, 0, s, a);
 }
 

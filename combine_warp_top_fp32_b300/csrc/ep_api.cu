@@ -360,6 +360,7 @@ ep_status_t ep_combine(const ep_config_t* cfg, const void* expert_out, const flo
   a.y = y;
   a.status = static_cast<uint32_t*>(ws);
   a.counter = reinterpret_cast<unsigned*>(static_cast<char*>(ws) + 64);  // the launcher may not use it
+  a.static_rounds = 1;
   return from_cuda(ep::launch_combine(a, sms, stream));
 }
 

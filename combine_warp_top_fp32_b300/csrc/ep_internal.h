@@ -257,6 +257,7 @@ struct CombineArgs {
   void* y;
   uint32_t* status;
   unsigned* counter;  // two words of the workspace (zero between calls): a unit counter and the warps done; or null
+  int static_rounds;  // with counter: units each warp takes in the static order before the shared ones (>= 1)
 };
 
 cudaError_t launch_combine(const CombineArgs& a, int sms, cudaStream_t s);
