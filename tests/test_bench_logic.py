@@ -110,3 +110,22 @@ def test_warmup_below_three_is_rejected():
 
     with pytest.raises(SystemExit):
         bench.parse_args(["--warmup", "2"])
+
+
+def test_combine_only_arguments_and_bytes():
+    """--combine-only parses a list of formats; with int8 expert outputs the
+    combine's bytes are the combine term of algorithmic_bytes (N*H read, N*4
+    scales, T*H*2 written), and int4 reads half the row bytes."""
+    import bench
+    from combine_warp_top_fp32_b300 import workloads
+
+    a = bench.parse_args(["--combine-only", "bf16,int8,fp8,int4", "--workload", "capacity"])
+    assert a.combine_only.split(",") == ["bf16", "int8", "fp8", "int4"]
+    w = workloads.WORKLOADS["capacity"]
+    N = 63_905
+    per = bench.PAYLOAD_BYTES
+    nb8 = bench.algorithmic_bytes(w.T, w.H, w.E, w.k, N, payload_int8=True, out_int8=True)
+    assert int(N * w.H * per["int8"]) + N * 4 + w.T * w.H * 2 == nb8["combine"]
+    nb16 = bench.algorithmic_bytes(w.T, w.H, w.E, w.k, N, payload_int8=True)
+    assert int(N * w.H * per["bf16"]) + w.T * w.H * 2 == nb16["combine"]
+    assert int(N * w.H * per["int4"]) * 2 == int(N * w.H * per["int8"])
